@@ -1,0 +1,395 @@
+/*
+ * hdp_oracle.c -- plain, slow, fp64 CPU oracle for document-masked causal
+ * attention over a packed micro-batch cut into capacity-C chunks.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or helper with the CUDA path.
+ *
+ * Source: "ByteScale: Communication-Efficient Scaling of LLM Training with a
+ * 2048K Context Length on 16384 GPUs" (AI training network primer research
+ * digest).
+ *   - capacity C and the ceil(s/C) ranks of a sequence: section 1 and
+ *     section 3.1 (Figure 2);
+ *   - short sequences packed onto one rank by best fit: section 3.1,
+ *     Figure 2(b);
+ *   - a query attends only to its own sequence; one C x C block per ring step,
+ *     partial results combined across steps: section 3.2;
+ *   - attention time grows as O(s^2): section 1, section 2.
+ *
+ * Everything is written as the plain definition: explicit loops in fp64,
+ * exact two-pass softmax per (query, head), no tiling, no online rescaling.
+ * Readings where the pages are silent (best-fit-decreasing tie-breaks, shard
+ * numbering, natural-log LSE, consecutive GQA grouping) are stated next to
+ * the code that takes them.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL 1
+#define ORC_ENOMEM 2
+
+/* bf16 bit pattern -> double, exactly (a bf16 is the top half of an fp32). */
+static double bf16_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* ------------------------------------------------------------------ plan */
+
+/* Number of chunks of a sequence of length s at capacity C, counted by
+ * walking the sequence C tokens at a time (section 3.1: a sequence longer than
+ * C spans ceil(s/C) ranks). */
+static int32_t count_chunks(int32_t s, int32_t C) {
+  int32_t n = 0;
+  for (int64_t t = 0; t < s; t += C) n++;
+  return n;
+}
+
+/* Totals needed to size the plan tables. */
+int oracle_plan_sizes(const int32_t* lengths, int32_t n, int32_t C, int32_t* num_chunks, int64_t* num_blocks,
+                      int64_t* total_tokens) {
+  if (n < 0 || C < 1) return ORC_EINVAL;
+  int64_t nc = 0, nb = 0, tt = 0;
+  for (int32_t i = 0; i < n; i++) {
+    if (lengths[i] < 1) return ORC_EINVAL;
+    int32_t c = count_chunks(lengths[i], C);
+    nc += c;
+    /* blocks (qc, kc) with 0 <= kc <= qc < c, counted one by one */
+    for (int32_t qc = 0; qc < c; qc++)
+      for (int32_t kc = 0; kc <= qc; kc++) nb++;
+    tt += lengths[i];
+  }
+  *num_chunks = (int32_t)nc;
+  *num_blocks = nb;
+  *total_tokens = tt;
+  return ORC_OK;
+}
+
+/* Piece of a sequence shorter than C, to be packed by best fit. */
+typedef struct {
+  int32_t len, doc, chunk;
+} piece_t;
+
+/* Best-fit-decreasing order: length descending, then document ascending. */
+static int piece_cmp(const void* a, const void* b) {
+  const piece_t* x = (const piece_t*)a;
+  const piece_t* y = (const piece_t*)b;
+  if (x->len != y->len) return x->len > y->len ? -1 : 1;
+  return x->doc < y->doc ? -1 : (x->doc > y->doc ? 1 : 0);
+}
+
+/*
+ * The sharding plan.
+ *   cu_seqlens[n+1]    exclusive prefix sum of lengths (token offsets)
+ *   chunk_offsets[n+1] exclusive prefix sum of chunks per sequence
+ *   block_offsets[n+1] exclusive prefix sum of causal (qc, kc) blocks per sequence
+ *   chunk_table[Nc][4] {doc, index within doc, first global token, length}
+ *   block_table[Nb][2] {global q chunk, global kv chunk}, ordered by doc, then
+ *                      q chunk, then kv chunk ascending
+ *   chunk_pairs[Nc]    causal (query, key) pairs whose query lies in the chunk
+ *   shard_of_chunk[Nc] rank ("shard") holding the chunk
+ *
+ * Shards (section 3.1, Figure 2(b): full C-token slices get a rank each,
+ * shorter sequences are packed onto one rank by best fit).  Reading: every
+ * chunk of exactly C tokens gets its own shard, numbered in chunk order; then
+ * each piece shorter than C (a short sequence or the tail of a long one),
+ * taken in best-fit-decreasing order (length desc, doc asc), goes to the
+ * open piece shard with the least remaining capacity that still fits, the
+ * lowest shard id on ties, or else opens a new shard.
+ */
+int oracle_plan(const int32_t* lengths, int32_t n, int32_t C, int32_t* cu_seqlens, int32_t* chunk_offsets,
+                int64_t* block_offsets, int32_t* chunk_table, int32_t* block_table, int64_t* chunk_pairs,
+                int32_t* shard_of_chunk, int32_t* num_shards) {
+  if (n < 0 || C < 1) return ORC_EINVAL;
+  int64_t tok = 0, ch = 0, blk = 0;
+  for (int32_t i = 0; i < n; i++) {
+    if (lengths[i] < 1) return ORC_EINVAL;
+    cu_seqlens[i] = (int32_t)tok;
+    chunk_offsets[i] = (int32_t)ch;
+    block_offsets[i] = blk;
+    const int32_t s = lengths[i];
+    const int64_t first_chunk = ch;
+    int32_t idx = 0;
+    for (int64_t a = 0; a < s; a += C, idx++) {
+      int64_t b = a + C < s ? a + C : s;
+      chunk_table[ch * 4 + 0] = i;
+      chunk_table[ch * 4 + 1] = idx;
+      chunk_table[ch * 4 + 2] = (int32_t)(tok + a);
+      chunk_table[ch * 4 + 3] = (int32_t)(b - a);
+      /* doc-local query p sees keys 0..p: p+1 pairs */
+      int64_t pairs = 0;
+      for (int64_t p = a; p < b; p++) pairs += p + 1;
+      chunk_pairs[ch] = pairs;
+      ch++;
+    }
+    for (int32_t qc = 0; qc < idx; qc++)
+      for (int32_t kc = 0; kc <= qc; kc++) {
+        block_table[blk * 2 + 0] = (int32_t)(first_chunk + qc);
+        block_table[blk * 2 + 1] = (int32_t)(first_chunk + kc);
+        blk++;
+      }
+    tok += s;
+  }
+  cu_seqlens[n] = (int32_t)tok;
+  chunk_offsets[n] = (int32_t)ch;
+  block_offsets[n] = blk;
+
+  /* shards: full chunks first, in chunk order */
+  int32_t ns = 0;
+  int64_t npieces = 0;
+  for (int64_t c = 0; c < ch; c++) {
+    if (chunk_table[c * 4 + 3] == C)
+      shard_of_chunk[c] = ns++;
+    else
+      npieces++;
+  }
+  if (npieces > 0) {
+    piece_t* pcs = (piece_t*)malloc(sizeof(piece_t) * (size_t)npieces);
+    int64_t* remaining = (int64_t*)malloc(sizeof(int64_t) * (size_t)npieces);
+    int32_t* shard_id = (int32_t*)malloc(sizeof(int32_t) * (size_t)npieces);
+    if (!pcs || !remaining || !shard_id) {
+      free(pcs);
+      free(remaining);
+      free(shard_id);
+      return ORC_ENOMEM;
+    }
+    int64_t k = 0;
+    for (int64_t c = 0; c < ch; c++)
+      if (chunk_table[c * 4 + 3] != C) {
+        pcs[k].len = chunk_table[c * 4 + 3];
+        pcs[k].doc = chunk_table[c * 4 + 0];
+        pcs[k].chunk = (int32_t)c;
+        k++;
+      }
+    qsort(pcs, (size_t)npieces, sizeof(piece_t), piece_cmp);
+    int64_t nopen = 0; /* open piece shards, in order of opening (ascending id) */
+    for (int64_t p = 0; p < npieces; p++) {
+      int64_t best = -1;
+      for (int64_t s = 0; s < nopen; s++)
+        if (remaining[s] >= pcs[p].len && (best < 0 || remaining[s] < remaining[best])) best = s;
+      if (best < 0) {
+        best = nopen++;
+        remaining[best] = C;
+        shard_id[best] = ns++;
+      }
+      remaining[best] -= pcs[p].len;
+      shard_of_chunk[pcs[p].chunk] = shard_id[best];
+    }
+    free(pcs);
+    free(remaining);
+    free(shard_id);
+  }
+  *num_shards = ns;
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ FLOPs */
+
+/* Useful causal attention FLOPs: for every (query, key) pair with the key at
+ * or before the query in the same sequence, d multiply-adds for q.k and d for
+ * p.v (2 FLOPs each), per query head: 4*d*Hq per pair.  Pairs are counted
+ * one by one. */
+int64_t oracle_flops_total(const int32_t* lengths, int32_t n, int32_t d, int32_t hq) {
+  int64_t pairs = 0;
+  for (int32_t i = 0; i < n; i++)
+    for (int64_t p = 0; p < lengths[i]; p++) pairs += p + 1;
+  return pairs * 4 * (int64_t)d * hq;
+}
+
+/* Per-shard FLOPs: each chunk's pairs, times 4*d*Hq, summed into its shard. */
+int oracle_flops_per_shard(const int64_t* chunk_pairs, const int32_t* shard_of_chunk, int32_t num_chunks,
+                           int32_t num_shards, int32_t d, int32_t hq, int64_t* out) {
+  for (int32_t s = 0; s < num_shards; s++) out[s] = 0;
+  for (int32_t c = 0; c < num_chunks; c++) {
+    int32_t s = shard_of_chunk[c];
+    if (s < 0 || s >= num_shards) return ORC_EINVAL;
+    out[s] += chunk_pairs[c] * 4 * (int64_t)d * hq;
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ attention */
+
+/* Document containing global token t (cu_seqlens ascending). */
+static int32_t doc_of_token(const int32_t* cu, int32_t n, int64_t t) {
+  int32_t lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int32_t mid = (lo + hi + 1) / 2;
+    if (cu[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+/*
+ * Attention of one query row against the keys of its own document whose
+ * doc-local position j satisfies key_lo <= j < key_hi and j <= p (causal).
+ * With key_lo = 0 and key_hi = s this is the full row; a narrower range is a
+ * partial block of the ring step in section 3.2.  An empty range gives
+ * lse = -inf and o = 0.
+ *   scores  S_j = scale * sum_c q[c] k_j[c]
+ *   lse     = m + ln sum_j exp(S_j - m),  m = max_j S_j
+ *   o       = sum_j exp(S_j - lse) v_j
+ * Layouts: q [T][hq][d], k and v [T][hkv][d] (bf16 bits); query head h reads
+ * kv head h / (hq / hkv) (consecutive grouping).
+ */
+static void attend_row(const uint16_t* q, const uint16_t* k, const uint16_t* v, int32_t hq, int32_t hkv,
+                       int32_t d, double scale, int64_t doc_start, int64_t p, int32_t h, int64_t key_lo,
+                       int64_t key_hi, double* o, double* lse, double* scores) {
+  const int32_t g = h / (hq / hkv);
+  const uint16_t* qrow = q + ((doc_start + p) * hq + h) * (int64_t)d;
+  int64_t hi = key_hi < p + 1 ? key_hi : p + 1;
+  for (int32_t c = 0; c < d; c++) o[c] = 0.0;
+  if (key_lo >= hi) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t j = key_lo; j < hi; j++) {
+    const uint16_t* krow = k + ((doc_start + j) * hkv + g) * (int64_t)d;
+    double s = 0.0;
+    for (int32_t c = 0; c < d; c++) s += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+    s *= scale;
+    scores[j - key_lo] = s;
+    if (s > m) m = s;
+  }
+  double sum = 0.0;
+  for (int64_t j = key_lo; j < hi; j++) sum += exp(scores[j - key_lo] - m);
+  const double L = m + log(sum);
+  for (int64_t j = key_lo; j < hi; j++) {
+    const double w = exp(scores[j - key_lo] - L);
+    const uint16_t* vrow = v + ((doc_start + j) * hkv + g) * (int64_t)d;
+    for (int32_t c = 0; c < d; c++) o[c] += w * bf16_to_double(vrow[c]);
+  }
+  *lse = L;
+}
+
+static int check_heads(int32_t hq, int32_t hkv, int32_t d) {
+  if (hq < 1 || hkv < 1 || d < 1 || hq % hkv != 0) return ORC_EINVAL;
+  return ORC_OK;
+}
+
+/*
+ * Full document-masked causal attention over the packed batch.
+ *   o   [T][hq][d]  fp64 (not rounded)
+ *   lse [hq][T]     fp64, natural log
+ */
+int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* cu_seqlens,
+                     int32_t n, int32_t hq, int32_t hkv, int32_t d, double scale, double* o, double* lse) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; i++)
+    if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen) maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!scores) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t w = 0; w < T * hq; w++) {
+        const int64_t t = w / hq;
+        const int32_t h = (int32_t)(w % hq);
+        const int32_t i = doc_of_token(cu_seqlens, n, t);
+        const int64_t start = cu_seqlens[i];
+        const int64_t s = cu_seqlens[i + 1] - start;
+        attend_row(q, k, v, hq, hkv, d, scale, start, t - start, h, 0, s, o + (t * hq + h) * (int64_t)d,
+                   lse + (int64_t)h * T + t, scores);
+      }
+      free(scores);
+    }
+  }
+  return err;
+}
+
+/*
+ * Sampled rows: for sample i, query token tokens[i] with head heads[i],
+ * restricted to doc-local keys [key_lo[i], key_hi[i]) (pass NULL for the
+ * whole document).  o_out [ns][d], lse_out [ns].
+ */
+int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* cu_seqlens,
+                          int32_t n, int32_t hq, int32_t hkv, int32_t d, double scale, const int64_t* tokens,
+                          const int32_t* heads, const int64_t* key_lo, const int64_t* key_hi, int64_t ns,
+                          double* o_out, double* lse_out) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  for (int64_t i = 0; i < ns; i++)
+    if (tokens[i] < 0 || tokens[i] >= T || heads[i] < 0 || heads[i] >= hq) return ORC_EINVAL;
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; i++)
+    if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen) maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!scores) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t i = 0; i < ns; i++) {
+        const int64_t t = tokens[i];
+        const int32_t di = doc_of_token(cu_seqlens, n, t);
+        const int64_t start = cu_seqlens[di];
+        const int64_t s = cu_seqlens[di + 1] - start;
+        const int64_t lo = key_lo ? key_lo[i] : 0;
+        const int64_t hi = key_hi ? key_hi[i] : s;
+        attend_row(q, k, v, hq, hkv, d, scale, start, t - start, heads[i], lo < 0 ? 0 : lo, hi > s ? s : hi,
+                   o_out + i * (int64_t)d, lse_out + i, scores);
+      }
+      free(scores);
+    }
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------ merge */
+
+/*
+ * Exact log-sum-exp combination of m partial results of the same rows
+ * (section 3.2: partial blocks from each ring step are combined):
+ *   M   = max_k lse_k
+ *   lse = M + ln sum_k exp(lse_k - M)
+ *   o   = sum_k exp(lse_k - lse) o_k
+ * A partial with lse_k = -inf contributes nothing; if all are -inf the row's
+ * lse is -inf and o is 0.
+ * o_parts [m][rows][d], lse_parts [m][rows]; o_out [rows][d], lse_out [rows].
+ */
+int oracle_merge(int32_t m, int64_t rows, int32_t d, const double* o_parts, const double* lse_parts, double* o_out,
+                 double* lse_out) {
+  if (m < 1 || rows < 0 || d < 1) return ORC_EINVAL;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; r++) {
+    double M = -INFINITY;
+    for (int32_t k = 0; k < m; k++)
+      if (lse_parts[k * rows + r] > M) M = lse_parts[k * rows + r];
+    double* o = o_out + r * (int64_t)d;
+    for (int32_t c = 0; c < d; c++) o[c] = 0.0;
+    if (M == -INFINITY) {
+      lse_out[r] = -INFINITY;
+      continue;
+    }
+    double sum = 0.0;
+    for (int32_t k = 0; k < m; k++) sum += exp(lse_parts[k * rows + r] - M);
+    const double L = M + log(sum);
+    for (int32_t k = 0; k < m; k++) {
+      const double w = exp(lse_parts[k * rows + r] - L);
+      if (w == 0.0) continue;
+      const double* ok = o_parts + (k * rows + r) * (int64_t)d;
+      for (int32_t c = 0; c < d; c++) o[c] += w * ok[c];
+    }
+    lse_out[r] = L;
+  }
+  return ORC_OK;
+}
