@@ -1,0 +1,198 @@
+/*
+ * hdpattn.h -- C ABI of libhdpattn.so: document-masked causal attention over
+ * a packed, mixed-length micro-batch, with the sequences cut into chunks of at
+ * most C tokens, the causal (query chunk, key chunk) blocks computed as partial
+ * (O, LSE) results, and the partials merged exactly by log-sum-exp.  One GPU
+ * (sm_103a); everything runs in this library's CUDA kernels.
+ *
+ * Source of the method: "ByteScale: Communication-Efficient Scaling of LLM
+ * Training with a 2048K Context Length on 16384 GPUs" (AI training network
+ * primer research digest):
+ *   section 1      capacity C: each rank holds at most C tokens;
+ *   section 2      attention work grows as the square of each sequence length,
+ *                  so equal-token micro-batches carry unequal FLOPs;
+ *   section 3.1    a sequence longer than C spans ceil(s/C) ranks, shorter ones
+ *                  are packed onto one rank by best fit (Figure 2);
+ *   section 3.2    a query attends only to its own sequence; each ring step
+ *                  computes one C x C block whose partial results are combined.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* and every tensor argument are DEVICE pointers on the
+ *     current CUDA device; other pointers are host pointers.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All work is enqueued asynchronously on it; the only call that blocks the
+ *     host is hdp_plan_create (one small device-to-host read of totals) and
+ *     hdp_device_status (which synchronizes the stream by design).
+ *   - The caller owns every buffer it passes and must keep it alive until the
+ *     stream has finished the work.  A plan owns its tables.
+ *   - Errors are reported only through the return code; nothing aborts and no
+ *     exception crosses the ABI.  hdp_last_error_message() gives a thread-local
+ *     human-readable reason for the last failing call on this thread.
+ *   - Layouts: Q and O are [T][hq][d] bf16, K and V are [T][hkv][d] bf16, all
+ *     row-major and contiguous; LSE is [hq][T] fp32 in natural log.  Query head
+ *     h reads key/value head h / (hq / hkv).  T = total tokens, at most 2^31-1.
+ */
+#ifndef HDPATTN_H_
+#define HDPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HDP_OK = 0,
+  HDP_ERR_INVALID_ARGUMENT = 1, /* a documented precondition does not hold   */
+  HDP_ERR_UNSUPPORTED = 2,      /* valid, but outside what the kernels cover  */
+  HDP_ERR_OUT_OF_MEMORY = 3,    /* a device allocation failed                 */
+  HDP_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed          */
+  HDP_ERR_DEVICE_TIMEOUT = 5    /* a kernel's bounded wait expired (see hdp_device_status) */
+} hdp_status_t;
+
+/* Attention modes. */
+#define HDP_MODE_FUSED 0 /* every query tile runs over all its causal-prior key
+                            tiles; the chunk partials are merged in registers
+                            by the online softmax (exactly the LSE merge) */
+#define HDP_MODE_SPLIT 1 /* each causal block (qc, kc) is written as a partial
+                            (O, LSE) to the workspace, then hdp_lse_merge runs */
+
+/* Plan creation flags. */
+#define HDP_PLAN_DEFAULT 0u
+#define HDP_PLAN_NO_SHARDS 1u /* skip best-fit shard packing (num_shards = 0,
+                                 shard_of_chunk = NULL); for callers that only
+                                 need the attention tables */
+
+typedef struct hdp_plan_s* hdp_plan_t;
+
+/* Read-only view of a plan.  All table pointers are device pointers owned by
+ * the plan; they stay valid until hdp_plan_destroy. */
+typedef struct {
+  int32_t num_docs;      /* n                                                  */
+  int32_t capacity;      /* C                                                  */
+  int32_t num_chunks;    /* N_c = sum_i ceil(s_i / C)                          */
+  int32_t num_shards;    /* shards after packing (0 with HDP_PLAN_NO_SHARDS)   */
+  int64_t num_blocks;    /* N_b = sum_i n_i (n_i + 1) / 2 causal (qc, kc) blocks */
+  int64_t total_tokens;  /* T                                                  */
+  int32_t max_doc_len;   /* longest document                                   */
+  int32_t tile;          /* query/key tile rows used by the work lists (128)   */
+  const int32_t* cu_seqlens;     /* [n+1] exclusive prefix sum of lengths       */
+  const int32_t* chunk_offsets;  /* [n+1] first global chunk of each document   */
+  const int64_t* block_offsets;  /* [n+1] first block of each document          */
+  const int32_t* chunk_table;    /* [N_c][4] {doc, index in doc, first token, length} */
+  const int32_t* block_table;    /* [N_b][2] {q chunk, kv chunk}, ordered by doc,
+                                    then q chunk, then kv chunk ascending      */
+  const int64_t* chunk_pairs;    /* [N_c] causal (query, key) pairs per chunk  */
+  const int32_t* shard_of_chunk; /* [N_c] shard of each chunk (NULL if skipped) */
+  /* Query-tile work lists, heaviest first (weight descending, then
+   * enumeration order).  Rows of 8 int32: {q_row0, q_rows, kv_row0, kv_len,
+   * block (-1 in the fused list), row offset inside the query chunk, weight =
+   * key tiles, 0}.  Fully masked (cross-document or future) tiles never appear. */
+  const int32_t* tiles_fused;    /* [num_tiles_fused][8] one per document query tile */
+  int64_t num_tiles_fused;
+  const int32_t* tiles_split;    /* [num_tiles_split][8] one per block query tile
+                                    (NULL unless C is a multiple of `tile`)   */
+  int64_t num_tiles_split;
+} hdp_plan_view_t;
+
+/*
+ * Sharding plan (section 3.1, Figure 2): chunk every document into
+ * ceil(s/C) chunks of at most C tokens, enumerate the causal blocks
+ * (qc, kc), kc <= qc, of each document, count the causal pairs of each chunk,
+ * pack the chunks into shards (every full C-token chunk gets its own shard in
+ * chunk order; shorter pieces -- short documents and tails -- are packed by
+ * best-fit decreasing: length descending, document ascending, each into the
+ * open piece shard with the least remaining capacity that fits, lowest id on
+ * ties, else a new shard), and build the query-tile work lists.
+ *   d_lengths  [num_docs] int32 device array, every entry >= 1.
+ *   num_docs   >= 1.      capacity >= 1.
+ *   flags      HDP_PLAN_DEFAULT or HDP_PLAN_NO_SHARDS.
+ *   out        receives the plan (NULL on failure).
+ * Blocks the host once to read the totals.  Fails with INVALID_ARGUMENT for a
+ * length < 1 or T >= 2^31, UNSUPPORTED when more than 65,536 sub-capacity
+ * pieces need best-fit packing (use HDP_PLAN_NO_SHARDS), OUT_OF_MEMORY if the
+ * tables cannot be allocated.  Tables are allocated stream-ordered on
+ * `stream`.
+ */
+hdp_status_t hdp_plan_create(const int32_t* d_lengths, int32_t num_docs, int32_t capacity, void* stream,
+                             hdp_plan_t* out);
+hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num_docs, int32_t capacity, uint32_t flags,
+                                void* stream, hdp_plan_t* out);
+hdp_status_t hdp_plan_view(hdp_plan_t plan, hdp_plan_view_t* view);
+/* Frees the plan's tables, stream-ordered on the stream the plan was created
+ * on; work on other streams that uses the plan must be ordered before it. */
+hdp_status_t hdp_plan_destroy(hdp_plan_t plan);
+
+/*
+ * Workspace bytes hdp_attention_fwd needs for (plan, hq, d, mode).  FUSED needs
+ * none (0).  SPLIT needs the partials: N_b * C * hq * (d + 1) * 4 bytes, laid
+ * out as o_part [N_b][C][hq][d] fp32 followed by lse_part [N_b][hq][C] fp32
+ * (256-byte aligned), the format hdp_lse_merge reads.
+ */
+hdp_status_t hdp_attention_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t d, int32_t mode, size_t* bytes);
+
+/*
+ * Document-masked causal attention forward (section 3.2): for every document,
+ * query head h and doc-local query p,
+ *   S_j = scale * q_p . k_j for doc-local keys j <= p,
+ *   lse = ln sum_j exp(S_j),  o = sum_j exp(S_j - lse) v_j,
+ * with query tiles scheduled heaviest first and fully masked tiles skipped.
+ *   q [T][hq][d], k/v [T][hkv][d] bf16; o [T][hq][d] bf16 (round to nearest
+ *   even); lse [hq][T] fp32 (natural log).
+ *   hq % hkv == 0; d == 64 or 128 (else UNSUPPORTED); scale > 0.
+ *   FUSED: o and lse are final.  SPLIT: needs capacity % 128 == 0 and a
+ *   workspace of hdp_attention_workspace_bytes; writes the partials there,
+ *   then merges them into o and lse with hdp_lse_merge on the same stream.
+ *   q, k, v, o must be 16-byte aligned.
+ * Device-side wait timeouts are reported by hdp_device_status.
+ */
+hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, const void* v, int32_t hq,
+                               int32_t hkv, int32_t d, float scale, int32_t mode, void* workspace,
+                               size_t workspace_bytes, void* o, float* lse, void* stream);
+
+/*
+ * Exact log-sum-exp merge of the causal blocks of every query chunk
+ * (section 3.2: the partial results of the ring steps are combined):
+ *   M = max_k lse_k, lse = M + ln sum_k exp(lse_k - M), o = sum_k exp(lse_k - lse) o_k
+ * over the blocks (qc, kc), kc = 0..qc, of the chunk.
+ *   o_part [N_b][C][hq][d] fp32, lse_part [N_b][hq][C] fp32 (the SPLIT
+ *   workspace layout); o [T][hq][d] bf16, lse [hq][T] fp32.  d == 64 or 128.
+ */
+hdp_status_t hdp_lse_merge(hdp_plan_t plan, const float* o_part, const float* lse_part, int32_t hq, int32_t d,
+                           void* o, float* lse, void* stream);
+
+/*
+ * The same merge on plain arrays: m partials of `rows` rows of d values.
+ *   o_parts [m][rows][d] fp32, lse_parts [m][rows] fp32 -> o [rows][d] bf16,
+ *   lse [rows] fp32.  A partial with lse = -inf contributes nothing; a row whose
+ *   partials are all -inf gets lse = -inf and o = 0.  m >= 1, d % 4 == 0,
+ *   d <= 256.
+ */
+hdp_status_t hdp_lse_merge_rows(int32_t m, int64_t rows, int32_t d, const float* o_parts, const float* lse_parts,
+                                void* o, float* lse, void* stream);
+
+/*
+ * Useful causal-attention FLOPs per shard (section 2: micro-batches of equal
+ * tokens differ in FLOPs): d_out[s] = sum over the shard's chunks of
+ * 4 * d * hq * chunk_pairs, exact in int64.  d_out [num_shards] int64 device.
+ * INVALID_ARGUMENT if the plan was created with HDP_PLAN_NO_SHARDS.
+ */
+hdp_status_t hdp_flops_per_shard(hdp_plan_t plan, int32_t d, int32_t hq, int64_t* d_out, void* stream);
+
+/*
+ * Synchronizes `stream` and reports (then clears) a device-side failure
+ * recorded by an earlier kernel of this library on the current device:
+ * HDP_ERR_DEVICE_TIMEOUT when a bounded wait expired, HDP_ERR_CUDA when the
+ * stream reports a CUDA error, else HDP_OK.
+ */
+hdp_status_t hdp_device_status(void* stream);
+
+const char* hdp_status_string(hdp_status_t status);
+const char* hdp_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HDPATTN_H_ */

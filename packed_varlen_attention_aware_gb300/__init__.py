@@ -1,0 +1,61 @@
+"""GB300 (sm_103a) document-masked causal attention over packed, chunked
+micro-batches -- the local attention step of ByteScale's hybrid data
+parallelism ("ByteScale: Communication-Efficient Scaling of LLM Training with
+a 2048K Context Length on 16384 GPUs", research digest, sections 3.1-3.2).
+
+The compute path is libhdpattn.so (include/hdpattn.h); this package is its
+ctypes binding plus seeded workload generators.  Importing the package does
+not load the library; the first call does, and fails loudly if it is absent.
+"""
+from __future__ import annotations
+
+import math
+
+from .binding import (  # noqa: F401
+    EXPORTED,
+    HDP_ERR_CUDA,
+    HDP_ERR_DEVICE_TIMEOUT,
+    HDP_ERR_INVALID_ARGUMENT,
+    HDP_ERR_OUT_OF_MEMORY,
+    HDP_ERR_UNSUPPORTED,
+    HDP_MODE_FUSED,
+    HDP_MODE_SPLIT,
+    HDP_OK,
+    HDP_PLAN_DEFAULT,
+    HDP_PLAN_NO_SHARDS,
+    HdpError,
+    Plan,
+    hdp_attention_fwd,
+    hdp_attention_workspace_bytes,
+    hdp_device_status,
+    hdp_flops_per_shard,
+    hdp_last_error_message,
+    hdp_lse_merge,
+    hdp_lse_merge_rows,
+    hdp_plan_create,
+    hdp_status_string,
+    load,
+)
+
+
+def attention(q, k, v, d_lengths, capacity: int, mode: int = HDP_MODE_FUSED, scale: float | None = None,
+              plan: Plan | None = None, stream=None):
+    """Convenience wrapper: plan (unless given), attention, and (in SPLIT mode)
+    the merge.  q [T][hq][d], k/v [T][hkv][d] bf16 CUDA tensors; returns
+    (o bf16 [T][hq][d], lse fp32 [hq][T], plan)."""
+    import torch
+
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if plan is None:
+        plan = hdp_plan_create(d_lengths, capacity, stream=stream)
+    o = torch.empty_like(q)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    ws = None
+    nbytes = hdp_attention_workspace_bytes(plan, hq, d, mode)
+    if nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    hdp_attention_fwd(plan, q, k, v, hq, hkv, d, scale, mode, ws, o, lse, stream=stream)
+    return o, lse, plan

@@ -1,0 +1,231 @@
+"""ctypes binding of libhdpattn.so with the C ABI's names (include/hdpattn.h).
+
+Argument marshalling only: torch tensors are passed as device pointers and
+every step runs in the library's CUDA kernels.  There is no fallback: if the
+shared library is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libhdpattn.so")
+
+HDP_OK = 0
+HDP_ERR_INVALID_ARGUMENT = 1
+HDP_ERR_UNSUPPORTED = 2
+HDP_ERR_OUT_OF_MEMORY = 3
+HDP_ERR_CUDA = 4
+HDP_ERR_DEVICE_TIMEOUT = 5
+HDP_MODE_FUSED = 0
+HDP_MODE_SPLIT = 1
+HDP_PLAN_DEFAULT = 0
+HDP_PLAN_NO_SHARDS = 1
+
+# Every symbol include/hdpattn.h declares.
+EXPORTED = (
+    "hdp_plan_create", "hdp_plan_create_ex", "hdp_plan_view", "hdp_plan_destroy",
+    "hdp_attention_workspace_bytes", "hdp_attention_fwd", "hdp_lse_merge", "hdp_lse_merge_rows",
+    "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
+)
+
+
+class HdpError(RuntimeError):
+    def __init__(self, status: int, call: str, message: str):
+        self.status = status
+        super().__init__(f"{call} failed: status {status} ({message})")
+
+
+class PlanView(ctypes.Structure):
+    _fields_ = [
+        ("num_docs", ctypes.c_int32), ("capacity", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
+        ("num_shards", ctypes.c_int32), ("num_blocks", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
+        ("max_doc_len", ctypes.c_int32), ("tile", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p), ("chunk_offsets", ctypes.c_void_p), ("block_offsets", ctypes.c_void_p),
+        ("chunk_table", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("chunk_pairs", ctypes.c_void_p),
+        ("shard_of_chunk", ctypes.c_void_p), ("tiles_fused", ctypes.c_void_p), ("num_tiles_fused", ctypes.c_int64),
+        ("tiles_split", ctypes.c_void_p), ("num_tiles_split", ctypes.c_int64),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (once) and return the ctypes handle; raises if the library is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with packed_varlen_attention_aware_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        V, I32, I64, U32, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                     ctypes.c_float, ctypes.c_size_t)
+        sig = {
+            "hdp_plan_create": [V, I32, I32, V, V],
+            "hdp_plan_create_ex": [V, I32, I32, U32, V, V],
+            "hdp_plan_view": [V, ctypes.POINTER(PlanView)],
+            "hdp_plan_destroy": [V],
+            "hdp_attention_workspace_bytes": [V, I32, I32, I32, ctypes.POINTER(SZ)],
+            "hdp_attention_fwd": [V, V, V, V, I32, I32, I32, F32, I32, V, SZ, V, V, V],
+            "hdp_lse_merge": [V, V, V, I32, I32, V, V, V],
+            "hdp_lse_merge_rows": [I32, I64, I32, V, V, V, V, V],
+            "hdp_flops_per_shard": [V, I32, I32, V, V],
+            "hdp_device_status": [V],
+            "hdp_status_string": [ctypes.c_int],
+            "hdp_last_error_message": [],
+        }
+        for name, args in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        lib.hdp_status_string.restype = ctypes.c_char_p
+        lib.hdp_last_error_message.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int, call: str):
+    if status != HDP_OK:
+        msg = load().hdp_last_error_message().decode(errors="replace")
+        raise HdpError(status, call, msg)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class _DeviceArray:
+    """Zero-copy view of plan-owned device memory for torch.as_tensor."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+class Plan:
+    """Owner of an hdp_plan_t; tables are exposed as torch views (valid while the plan lives)."""
+
+    def __init__(self, handle: ctypes.c_void_p):
+        self._h = handle
+        v = PlanView()
+        _check(load().hdp_plan_view(self._h, ctypes.byref(v)), "hdp_plan_view")
+        self.view = v
+
+    @property
+    def handle(self):
+        return self._h
+
+    def _table(self, name, shape, typestr):
+        import torch
+
+        ptr = getattr(self.view, name)
+        if not ptr or 0 in shape:
+            dt = {"<i4": torch.int32, "<i8": torch.int64}[typestr]
+            return torch.zeros(shape, dtype=dt, device="cuda")
+        return torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
+
+    def tables(self) -> dict:
+        """Host copies (numpy) of every table of the plan."""
+        v = self.view
+        n, nc, nb = v.num_docs, v.num_chunks, v.num_blocks
+        out = {
+            "cu_seqlens": self._table("cu_seqlens", (n + 1,), "<i4"),
+            "chunk_offsets": self._table("chunk_offsets", (n + 1,), "<i4"),
+            "block_offsets": self._table("block_offsets", (n + 1,), "<i8"),
+            "chunk_table": self._table("chunk_table", (nc, 4), "<i4"),
+            "block_table": self._table("block_table", (nb, 2), "<i4"),
+            "chunk_pairs": self._table("chunk_pairs", (nc,), "<i8"),
+            "tiles_fused": self._table("tiles_fused", (v.num_tiles_fused, 8), "<i4"),
+        }
+        if v.shard_of_chunk:
+            out["shard_of_chunk"] = self._table("shard_of_chunk", (nc,), "<i4")
+        if v.tiles_split:
+            out["tiles_split"] = self._table("tiles_split", (v.num_tiles_split, 8), "<i4")
+        return {k: t.cpu().numpy() for k, t in out.items()}
+
+    def destroy(self):
+        if self._h:
+            h, self._h = self._h, None
+            _check(load().hdp_plan_destroy(h), "hdp_plan_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def hdp_plan_create(d_lengths, capacity: int, flags: int = HDP_PLAN_DEFAULT, stream=None) -> Plan:
+    """d_lengths: int32 CUDA tensor of document lengths."""
+    import torch
+
+    if d_lengths.dtype != torch.int32 or not d_lengths.is_cuda or not d_lengths.is_contiguous():
+        raise TypeError("d_lengths must be a contiguous int32 CUDA tensor")
+    h = ctypes.c_void_p()
+    _check(load().hdp_plan_create_ex(_ptr(d_lengths), d_lengths.numel(), int(capacity), int(flags),
+                                     _stream(stream), ctypes.byref(h)), "hdp_plan_create")
+    return Plan(h)
+
+
+def hdp_attention_workspace_bytes(plan: Plan, hq: int, d: int, mode: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().hdp_attention_workspace_bytes(plan.handle, hq, d, mode, ctypes.byref(n)),
+           "hdp_attention_workspace_bytes")
+    return int(n.value)
+
+
+def hdp_attention_fwd(plan: Plan, q, k, v, hq: int, hkv: int, d: int, scale: float, mode: int, workspace, o, lse,
+                      stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().hdp_attention_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), hq, hkv, d, float(scale), mode,
+                                    _ptr(workspace), ws_bytes, _ptr(o), _ptr(lse), _stream(stream)),
+           "hdp_attention_fwd")
+
+
+def hdp_lse_merge(plan: Plan, o_part, lse_part, hq: int, d: int, o, lse, stream=None):
+    _check(load().hdp_lse_merge(plan.handle, _ptr(o_part), _ptr(lse_part), hq, d, _ptr(o), _ptr(lse),
+                                _stream(stream)), "hdp_lse_merge")
+
+
+def hdp_lse_merge_rows(o_parts, lse_parts, o, lse, stream=None):
+    m, rows, d = o_parts.shape
+    _check(load().hdp_lse_merge_rows(m, rows, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse),
+                                     _stream(stream)), "hdp_lse_merge_rows")
+
+
+def hdp_flops_per_shard(plan: Plan, d: int, hq: int, d_out, stream=None):
+    _check(load().hdp_flops_per_shard(plan.handle, d, hq, _ptr(d_out), _stream(stream)), "hdp_flops_per_shard")
+
+
+def hdp_device_status(stream=None):
+    _check(load().hdp_device_status(_stream(stream)), "hdp_device_status")
+
+
+def hdp_status_string(status: int) -> str:
+    return load().hdp_status_string(status).decode()
+
+
+def hdp_last_error_message() -> str:
+    return load().hdp_last_error_message().decode(errors="replace")

@@ -1,0 +1,77 @@
+// Status strings, thread-local error messages and the device error word.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace {
+thread_local std::string g_last_error;
+__device__ unsigned int g_device_error;  // 0 = ok, else a code from the kernels
+
+std::mutex g_mu;
+unsigned int* g_err_ptr[64] = {nullptr};
+}  // namespace
+
+namespace hdp {
+
+hdp_status_t fail(hdp_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+hdp_status_t fail_cuda(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  if (e == cudaErrorMemoryAllocation) return HDP_ERR_OUT_OF_MEMORY;
+  return HDP_ERR_CUDA;
+}
+
+unsigned int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+}  // namespace hdp
+
+extern "C" {
+
+const char* hdp_status_string(hdp_status_t s) {
+  switch (s) {
+    case HDP_OK: return "HDP_OK";
+    case HDP_ERR_INVALID_ARGUMENT: return "HDP_ERR_INVALID_ARGUMENT";
+    case HDP_ERR_UNSUPPORTED: return "HDP_ERR_UNSUPPORTED";
+    case HDP_ERR_OUT_OF_MEMORY: return "HDP_ERR_OUT_OF_MEMORY";
+    case HDP_ERR_CUDA: return "HDP_ERR_CUDA";
+    case HDP_ERR_DEVICE_TIMEOUT: return "HDP_ERR_DEVICE_TIMEOUT";
+  }
+  return "HDP_ERR_UNKNOWN";
+}
+
+const char* hdp_last_error_message(void) { return g_last_error.c_str(); }
+
+hdp_status_t hdp_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  HDP_CUDA_TRY(cudaStreamSynchronize(s));
+  unsigned int* w = hdp::device_error_word();
+  if (!w) return hdp::fail(HDP_ERR_CUDA, "cannot resolve the device error word");
+  unsigned int code = 0, zero = 0;
+  HDP_CUDA_TRY(cudaMemcpyFromSymbol(&code, g_device_error, sizeof code));
+  if (code != 0) {
+    HDP_CUDA_TRY(cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero));
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "a kernel's bounded wait expired (code %u)", code);
+    return hdp::fail(HDP_ERR_DEVICE_TIMEOUT, buf);
+  }
+  return HDP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,591 @@
+// Document-masked causal attention forward on tcgen05 tensor cores
+// ("ByteScale: Communication-Efficient Scaling of LLM Training with a 2048K
+// Context Length on 16384 GPUs", research digest, section 3.2: a query attends
+// only to its own sequence; each C x C block of a long sequence is a partial
+// result, and partials are combined by log-sum-exp).
+//
+// Design (one persistent CTA per SM, 10 warps):
+//   warps 0-3  softmax for query slot 0     warps 4-7  softmax for query slot 1
+//   warp 8     TMA producer                 warp 9     MMA issuer + TMEM owner
+// A work unit is one query tile (128 rows of one document, from the plan's
+// heaviest-first work list) for one key/value head and a pair of query heads of
+// that head's GQA group: both slots share every K/V tile.  Only the key tiles
+// of the tile's causal range inside its own document are visited, so fully
+// masked tiles are never loaded or computed; the mask is applied only on the
+// tiles that straddle the diagonal or the end of the key range.
+//
+// Per key tile j and slot s:
+//   S_s = Q_s K_j^T        tcgen05.mma, A and B from 128B-swizzled smem, D in TMEM
+//   softmax_s              tcgen05.ld S, online max / exp2 / row sum in fp32,
+//                          P (bf16) written back into S's TMEM columns
+//   O_s += P_s V_j         tcgen05.mma with A = P from TMEM, B = V (MN-major smem)
+// The online softmax keeps a stale running max unless it grows by more than
+// 2^8, so O is rescaled only rarely; the final O/l and LSE use the same max, so
+// the result is exact.  In SPLIT mode each block (q chunk, kv chunk) ends in a
+// partial (O fp32, LSE) instead.
+//
+// Every mbarrier wait is bounded; a timeout sets the device error word, all
+// roles stop, in-flight copies and MMAs are drained, TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace hdp {
+
+hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, const float* lse_part, int32_t hq,
+                                 int32_t d, void* o, float* lse, cudaStream_t st);
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;  // K and V ring depth
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+// error codes recorded in the device error word
+constexpr int kErrQFull = 0x101, kErrKFull = 0x102, kErrVFull = 0x103, kErrSFull = 0x104, kErrPFull = 0x105,
+              kErrOFull = 0x106, kErrOEmpty = 0x107, kErrKEmpty = 0x108, kErrVEmpty = 0x109, kErrQEmpty = 0x10a;
+
+template <int D>
+struct SmemLayout {
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kHalfBytes = kTile * 64 * 2;  // one 64-column (128-byte) half
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kBytes = kBar + 512;
+};
+
+struct Bars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t drain;  // private to the MMA thread: completion of all its MMAs at exit
+  uint32_t tmem_base;
+  int abort_word;
+};
+
+struct Params {
+  const int32_t* tiles;  // [ntiles][8]
+  long long ntiles;
+  int hq, hkv, group, npairs;
+  float scale_log2;      // scale * log2(e)
+  long long T;
+  __nv_bfloat16* o;      // FUSED output [T][hq][D]
+  float* lse;            // FUSED output [hq][T]
+  float* o_part;         // SPLIT partials [N_b][C][hq][D]
+  float* lse_part;       // SPLIT partials [N_b][hq][C]
+  int C;
+  int split;
+  unsigned int* err;
+};
+
+struct Unit {
+  int q_row0, q_rows, kv_row0, kv_len, blk, row_off;
+  int kvh, h0;       // kv head, first query head of the pair
+  bool valid1;       // slot 1 in use
+  int ntiles_kv;
+};
+
+__device__ __forceinline__ Unit load_unit(const Params& p, long long u) {
+  const long long per_tile = static_cast<long long>(p.hkv) * p.npairs;
+  const long long ti = u / per_tile;
+  const int r = static_cast<int>(u - ti * per_tile);
+  const int4* row = reinterpret_cast<const int4*>(p.tiles + ti * 8);
+  const int4 a = __ldg(row), b = __ldg(row + 1);
+  Unit x;
+  x.q_row0 = a.x;
+  x.q_rows = a.y;
+  x.kv_row0 = a.z;
+  x.kv_len = a.w;
+  x.blk = b.x;
+  x.row_off = b.y;
+  x.kvh = r / p.npairs;
+  const int pair = r - x.kvh * p.npairs;
+  x.h0 = x.kvh * p.group + 2 * pair;
+  x.valid1 = 2 * pair + 1 < p.group;
+  x.ntiles_kv = (x.kv_len + kTile - 1) / kTile;
+  return x;
+}
+
+// Static snake schedule over the heaviest-first unit list.
+__device__ __forceinline__ long long unit_index(long long k, int cta, int nctas) {
+  const long long round = k / 1;  // one unit per CTA per round
+  return round * nctas + ((round & 1) ? (nctas - 1 - cta) : cta);
+}
+
+// Bounded wait used only while tearing down after an abort (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > kWaitBudgetClocks / 4) break;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = SmemLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bars = *reinterpret_cast<Bars*>(smem + L::kBar);
+  volatile int* abort_word = &bars.abort_word;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const long long total_units = p.ntiles * p.hkv * p.npairs;
+  const int cta = blockIdx.x, nctas = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.s_full[s], 1);
+      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.o_full[s], 1);
+      mbar_init(&bars.o_empty[s], 128);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort_word = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D); P_s aliases S_s[0,64)
+  auto tS = [tmem](int slot) { return tmem + static_cast<uint32_t>(slot) * 128u; };
+  auto tO = [tmem](int slot) { return tmem + 256u + static_cast<uint32_t>(slot) * D; };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t q_uses[2] = {0, 0};
+      uint32_t kcount[kStages] = {}, vcount[kStages] = {};  // loads issued per stage
+      long long kload = 0, vload = 0;
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long u = unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const Unit x = load_unit(p, u);
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (s == 1 && !x.valid1) continue;
+          if (q_uses[s] > 0) ok = mbar_wait(&bars.q_empty[s], (q_uses[s] - 1) & 1, abort_word, p.err, kErrQEmpty);
+          if (!ok) break;
+          ++q_uses[s];
+          uint8_t* dst = smem + L::kQ + s * L::kTileBytes;
+          mbar_arrive_expect_tx(&bars.q_full[s], L::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(dst + hb * L::kHalfBytes, &tmQ, &bars.q_full[s], hb * 64, x.h0 + s, x.q_row0);
+        }
+        for (int j = 0; j < x.ntiles_kv && ok; ++j) {
+          const int row = x.kv_row0 + j * kTile;
+          {
+            const int st = static_cast<int>(kload % kStages);
+            const long long round = kload / kStages;
+            if (round > 0) ok = mbar_wait(&bars.k_empty[st], (round - 1) & 1, abort_word, p.err, kErrKEmpty);
+            if (!ok) break;
+            uint8_t* dst = smem + L::kK + st * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars.k_full[st], L::kTileBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(dst + hb * L::kHalfBytes, &tmK, &bars.k_full[st], hb * 64, x.kvh, row);
+            ++kload;
+            ++kcount[st];
+          }
+          {
+            const int st = static_cast<int>(vload % kStages);
+            const long long round = vload / kStages;
+            if (round > 0) ok = mbar_wait(&bars.v_empty[st], (round - 1) & 1, abort_word, p.err, kErrVEmpty);
+            if (!ok) break;
+            uint8_t* dst = smem + L::kV + st * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars.v_full[st], L::kTileBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(dst + hb * L::kHalfBytes, &tmV, &bars.v_full[st], hb * 64, x.kvh, row);
+            ++vload;
+            ++vcount[st];
+          }
+        }
+      }
+      if (!ok) {
+        // drain: every armed full barrier completes once its bytes land
+        for (int st = 0; st < kStages; ++st) {
+          if (kcount[st] > 0) drain_wait(&bars.k_full[st], (kcount[st] - 1) & 1);
+          if (vcount[st] > 0) drain_wait(&bars.v_full[st], (vcount[st] - 1) & 1);
+        }
+        for (int s = 0; s < 2; ++s)
+          if (q_uses[s] > 0) drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+      uint32_t q_uses[2] = {0, 0}, pv_count[2] = {0, 0}, units_done[2] = {0, 0};
+      long long kuse = 0, vuse = 0;
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long u = unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const Unit x = load_unit(p, u);
+        const int nslots = x.valid1 ? 2 : 1;
+        for (int s = 0; s < nslots && ok; ++s) {
+          ok = mbar_wait(&bars.q_full[s], q_uses[s] & 1, abort_word, p.err, kErrQFull);
+          ++q_uses[s];
+        }
+        for (int j = 0; j < x.ntiles_kv && ok; ++j) {
+          const int kst = static_cast<int>(kuse % kStages);
+          ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
+          for (int s = 0; s < nslots && ok; ++s) {
+            // S_s aliases P_s of the previous P.V of this slot: wait for it
+            if (pv_count[s] > 0) ok = mbar_wait(&bars.o_full[s], (pv_count[s] - 1) & 1, abort_word, p.err, kErrOFull);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t qa = sQ + s * L::kTileBytes;
+            const uint32_t kb = sK + kst * L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+              umma_ss(tS(s), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+            }
+            umma_commit(&bars.s_full[s]);
+            if (j == x.ntiles_kv - 1) umma_commit(&bars.q_empty[s]);
+          }
+          if (!ok) break;
+          umma_commit(&bars.k_empty[kst]);
+          ++kuse;
+          const int vst = static_cast<int>(vuse % kStages);
+          ok = mbar_wait(&bars.v_full[vst], (vuse / kStages) & 1, abort_word, p.err, kErrVFull);
+          for (int s = 0; s < nslots && ok; ++s) {
+            // P_s(j) written (and O_s rescaled) by the softmax warps
+            ok = mbar_wait(&bars.p_full[s], pv_count[s] & 1, abort_word, p.err, kErrPFull);
+            // first P.V of a unit overwrites O_s: the previous epilogue must have read it
+            if (ok && j == 0 && units_done[s] > 0)
+              ok = mbar_wait(&bars.o_empty[s], (units_done[s] - 1) & 1, abort_word, p.err, kErrOEmpty);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vb = sV + vst * L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_ts(tO(s), tS(s) + kk * 8, sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bars.o_full[s]);
+            ++pv_count[s];
+          }
+          if (!ok) break;
+          umma_commit(&bars.v_empty[vst]);
+          ++vuse;
+        }
+        for (int s = 0; s < nslots; ++s) ++units_done[s];
+      }
+      // drain every MMA this thread issued before TMEM is released
+      umma_commit(&bars.drain);
+      drain_wait(&bars.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int s = warp >> 2;              // slot
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = tile row
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t s_count = 0, units_done = 0;
+    bool ok = true;
+    for (long long k = 0; ok; ++k) {
+      const long long u = unit_index(k, cta, nctas);
+      if (u >= total_units) break;
+      const Unit x = load_unit(p, u);
+      if (s == 1 && !x.valid1) continue;
+      const int h = x.h0 + s;
+      // doc-local query position relative to the first key of the range
+      const int q_rel = x.q_row0 - x.kv_row0 + row;
+      const int key_limit = min(q_rel + 1, x.kv_len);  // keys [0, key_limit) are allowed
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < x.ntiles_kv && ok; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[s], s_count & 1, abort_word, p.err, kErrSFull));
+        if (!ok) break;
+        ++s_count;
+        tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS(s) + lane_off + c * 32, r[c]);
+        tmem_wait_ld();
+        const int lim = key_limit - j * kTile;
+        if (lim < kTile) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[c][i]));
+        const float mt_scaled = mt * p.scale_log2;
+        bool rescale_o = false;
+        float alpha = 1.f;
+        if (mt_scaled > m + kRescaleThreshold || j == 0) {
+          const float m_new = fmaxf(m, mt_scaled);
+          alpha = (j == 0) ? 0.f : ex2_approx(m - m_new);
+          l *= alpha;
+          m = m_new;
+          rescale_o = j > 0;
+        }
+        const float neg_m = -m;
+        float rowsum = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][i]), p.scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), p.scale_log2, neg_m));
+            rowsum += p0 + p1;
+            pk[c >> 1][(c & 1) * 16 + i / 2] = pack_bf16x2(p0, p1);
+          }
+        l += rowsum;
+        tmem_st32(tS(s) + lane_off, pk[0]);
+        tmem_st32(tS(s) + lane_off + 32, pk[1]);
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // P.V of tile j-1 is complete: it finished before S_s(j) was computed
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO(s) + lane_off + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO(s) + lane_off + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[s]);
+      }
+      if (!ok) break;
+      // ---- epilogue: wait for the last P.V, normalize, store
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[s], (s_count - 1) & 1, abort_word, p.err, kErrOFull));
+      if (!ok) break;
+      tc_fence_after();
+      const bool row_valid = row < x.q_rows;
+      const float inv_l = 1.f / l;
+      const float lse_val = (m + __log2f(l)) * 0.69314718055994530942f;
+      const long long tok = static_cast<long long>(x.q_row0) + row;
+      if (!p.split) {
+        __nv_bfloat16* dst = p.o + (tok * p.hq + h) * static_cast<long long>(D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO(s) + lane_off + c * 32, o);
+          tmem_wait_ld();
+          if (row_valid) {
+            uint4 w[4];
+            uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              wp[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = w[i];
+          }
+        }
+        if (row_valid) p.lse[static_cast<long long>(h) * p.T + tok] = lse_val;
+      } else {
+        const long long prow = static_cast<long long>(x.blk) * p.C + x.row_off + row;
+        float* dst = p.o_part + (prow * p.hq + h) * static_cast<long long>(D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO(s) + lane_off + c * 32, o);
+          tmem_wait_ld();
+          if (row_valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                  __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        }
+        if (row_valid)
+          p.lse_part[(static_cast<long long>(x.blk) * p.hq + h) * p.C + x.row_off + row] = lse_val;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.o_empty[s]);
+      ++units_done;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [T][heads][d] bf16 viewed as a 3-D tensor (d, heads, T); box = 64 columns x
+// 1 head x 128 rows, 128-byte swizzle (the canonical K-major SW128 layout).
+hdp_status_t make_map(CUtensorMap* m, const void* base, long long T, int heads, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(HDP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HDP_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(r) + ")");
+  return HDP_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+template <int D>
+hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const void* v, int hq, int hkv,
+                    float scale, bool split, float* o_part, float* lse_part, void* o, float* lse, cudaStream_t st) {
+  const long long T = plan->v.total_tokens;
+  CUtensorMap mq, mk, mv;
+  hdp_status_t r;
+  if ((r = make_map(&mq, q, T, hq, D)) != HDP_OK) return r;
+  if ((r = make_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
+  if ((r = make_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
+  Params prm{};
+  prm.tiles = split ? plan->v.tiles_split : plan->v.tiles_fused;
+  prm.ntiles = split ? plan->v.num_tiles_split : plan->v.num_tiles_fused;
+  prm.hq = hq;
+  prm.hkv = hkv;
+  prm.group = hq / hkv;
+  prm.npairs = (prm.group + 1) / 2;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.T = T;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  prm.C = plan->v.capacity;
+  prm.split = split ? 1 : 0;
+  prm.err = device_error_word();
+  if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
+  const long long units = prm.ntiles * hkv * prm.npairs;
+  if (units == 0) return HDP_OK;
+  int dev = 0, sms = 0;
+  HDP_CUDA_TRY(cudaGetDevice(&dev));
+  HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  const int smem = SmemLayout<D>::kBytes + 1024;
+  HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  k_attn_fwd<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
+  HDP_CUDA_TRY(cudaGetLastError());
+  return HDP_OK;
+}
+
+hdp_status_t split_workspace(const hdp_plan_s* plan, int hq, int d, size_t* o_bytes, size_t* total) {
+  const size_t rows = static_cast<size_t>(plan->v.num_blocks) * plan->v.capacity;
+  *o_bytes = align256(rows * hq * d * sizeof(float));
+  *total = *o_bytes + align256(rows * hq * sizeof(float));
+  return HDP_OK;
+}
+
+}  // namespace
+}  // namespace hdp
+
+using namespace hdp;
+
+extern "C" hdp_status_t hdp_attention_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t d, int32_t mode,
+                                                      size_t* bytes) {
+  if (!plan || !bytes) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_workspace_bytes: NULL argument");
+  if (hq < 1 || d < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_workspace_bytes: hq, d must be >= 1");
+  if (mode == HDP_MODE_FUSED) {
+    *bytes = 0;
+    return HDP_OK;
+  }
+  if (mode != HDP_MODE_SPLIT) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_workspace_bytes: unknown mode");
+  size_t ob = 0;
+  return split_workspace(plan, hq, d, &ob, bytes);
+}
+
+extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, const void* v, int32_t hq,
+                                          int32_t hkv, int32_t d, float scale, int32_t mode, void* workspace,
+                                          size_t workspace_bytes, void* o, float* lse, void* stream) {
+  if (!plan || !q || !k || !v || !o || !lse) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: NULL argument");
+  if (hq < 1 || hkv < 1 || hq % hkv != 0)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: need hq >= 1, hkv >= 1, hq % hkv == 0");
+  if (!(scale > 0.f)) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: scale must be > 0");
+  if (mode != HDP_MODE_FUSED && mode != HDP_MODE_SPLIT)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: unknown mode");
+  if (d != 64 && d != 128) return fail(HDP_ERR_UNSUPPORTED, "hdp_attention_fwd: d must be 64 or 128");
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if (mis & 15) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: q, k, v, o must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool split = mode == HDP_MODE_SPLIT;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (split) {
+    if (plan->v.capacity % kTile != 0 || !plan->v.tiles_split)
+      return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT needs capacity % 128 == 0");
+    size_t ob = 0, need = 0;
+    split_workspace(plan, hq, d, &ob, &need);
+    if (!workspace || workspace_bytes < need)
+      return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT workspace too small (need " +
+                                                std::to_string(need) + " bytes)");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255)
+      return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: workspace must be 256-byte aligned");
+    o_part = static_cast<float*>(workspace);
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ob);
+  }
+  hdp_status_t r = d == 128 ? launch<128>(plan, q, k, v, hq, hkv, scale, split, o_part, lse_part, o, lse, st)
+                            : launch<64>(plan, q, k, v, hq, hkv, scale, split, o_part, lse_part, o, lse, st);
+  if (r != HDP_OK || !split) return r;
+  return launch_merge_blocks(plan, o_part, lse_part, hq, d, o, lse, st);
+}

@@ -1,0 +1,40 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/hdpattn.h"
+
+namespace hdp {
+
+constexpr int kTile = 128;             // query/key rows per attention tile
+constexpr int64_t kMaxPieces = 65536;  // best-fit packing limit (sub-capacity pieces)
+
+// Record a thread-local error message and return `st`.
+hdp_status_t fail(hdp_status_t st, const std::string& msg);
+hdp_status_t fail_cuda(cudaError_t e, const char* what);
+#define HDP_CUDA_TRY(expr)                          \
+  do {                                              \
+    cudaError_t e_ = (expr);                        \
+    if (e_ != cudaSuccess) return ::hdp::fail_cuda(e_, #expr); \
+  } while (0)
+
+// Device error word shared by all kernels (bounded-wait timeouts, internal
+// consistency checks).  Defined in api.cu; read by hdp_device_status.
+unsigned int* device_error_word();
+
+}  // namespace hdp
+
+struct hdp_plan_s {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  uint32_t flags = 0;
+  hdp_plan_view_t v{};
+  void* mem = nullptr;   // stream-ordered allocation holding the N_c/N_b/tile-sized tables
+  void* mem1 = nullptr;  // stream-ordered allocation holding the [n+1] offset arrays
+  // internal tables (inside `mem`)
+  const int64_t* tile_offsets_fused = nullptr;  // [n+1]
+  const int64_t* tile_offsets_split = nullptr;  // [n+1]
+};

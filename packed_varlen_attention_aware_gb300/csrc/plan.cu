@@ -1,0 +1,811 @@
+// Sharding plan, best-fit shard packing, query-tile work lists and per-shard
+// FLOPs ("ByteScale: Communication-Efficient Scaling of LLM Training with a
+// 2048K Context Length on 16384 GPUs", research digest, sections 1, 2, 3.1
+// and Figure 2).
+//
+// Kernels:
+//   k_plan_reduce / k_plan_scan_partials / k_plan_scan_write
+//       three-phase (reduce, scan of CTA sums, re-scan) warp-shuffle prefix
+//       sums of the per-document quantities: tokens, chunks ceil(s/C), causal
+//       blocks n(n+1)/2, fused query tiles, split query tiles, sub-capacity
+//       pieces.  Integer only, bit-exact.
+//   k_fill_chunks / k_fill_blocks / k_fill_tiles_*
+//       one thread per table row; the row's document is found by binary
+//       search over the scanned offsets, the rest is closed-form.
+//   k_bitonic_*   sort of 64-bit keys (work lists heaviest first, pieces in
+//                 best-fit-decreasing order).
+//   k_shard_bfd   one CTA: sequential best fit over the sorted pieces with a
+//                 block-wide argmin over the open shards.
+//   k_flops_*     exact int64 per-shard FLOPs.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <string>
+
+#include "internal.h"
+
+namespace hdp {
+namespace {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kScanThreads * kScanItems;  // documents per CTA
+constexpr int kQ = 6;  // tokens, chunks, blocks, fused tiles, split tiles, pieces
+constexpr int kPartial = 8;  // kQ sums + max length + invalid-length flag
+constexpr int kIdxBits = 40;
+constexpr unsigned long long kIdxMask = (1ull << kIdxBits) - 1;
+constexpr long long kWeightCap = 1ll << 24;  // > max tiles of a document (2^31 / 128)
+
+__device__ __forceinline__ void doc_quantities(int32_t s, int32_t C, bool split_ok, long long (&q)[kQ]) {
+  const long long n = (static_cast<long long>(s) + C - 1) / C;
+  q[0] = s;
+  q[1] = n;
+  q[2] = n * (n + 1) / 2;
+  q[3] = (static_cast<long long>(s) + kTile - 1) / kTile;
+  if (split_ok) {
+    const long long tpc = C / kTile;
+    const long long last = s - (n - 1) * static_cast<long long>(C);
+    const long long tl = (last + kTile - 1) / kTile;
+    q[4] = tpc * ((n - 1) * n / 2) + tl * n;
+  } else {
+    q[4] = 0;
+  }
+  q[5] = (s % C) != 0 ? 1 : 0;
+}
+
+// Exclusive scan of N int64 values over a 256-thread block; also returns the
+// block totals.  Warp level: shuffle-up inclusive scan; block level: scan of
+// the 8 warp sums by warp 0.
+template <int N>
+__device__ void block_exclusive_scan(long long (&x)[N], long long (&total)[N]) {
+  __shared__ long long wsum[kScanThreads / 32][N];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long inc[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) inc[i] = x[i];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const long long y = __shfl_up_sync(0xffffffffu, inc[i], off);
+      if (lane >= off) inc[i] += y;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) wsum[warp][i] = inc[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int W = kScanThreads / 32;
+    long long w[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = lane < W ? wsum[lane][i] : 0;
+#pragma unroll
+    for (int off = 1; off < W; off <<= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const long long y = __shfl_up_sync(0xffffffffu, w[i], off);
+        if (lane >= off) w[i] += y;
+      }
+    }
+    if (lane < W) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) wsum[lane][i] = w[i];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const long long before = warp > 0 ? wsum[warp - 1][i] : 0;
+    total[i] = wsum[kScanThreads / 32 - 1][i];
+    x[i] = before + inc[i] - x[i];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_plan_reduce(const int32_t* __restrict__ lengths, int32_t n,
+                                                              int32_t C, int split_ok,
+                                                              long long* __restrict__ partials) {
+  long long acc[kQ] = {0, 0, 0, 0, 0, 0};
+  long long mx = 0, bad = 0;
+  const long long base = static_cast<long long>(blockIdx.x) * kScanTile;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    const long long i = base + j * kScanThreads + threadIdx.x;  // coalesced
+    if (i < n) {
+      const int32_t s = lengths[i];
+      if (s < 1) {
+        bad = 1;
+      } else {
+        long long q[kQ];
+        doc_quantities(s, C, split_ok != 0, q);
+#pragma unroll
+        for (int k = 0; k < kQ; ++k) acc[k] += q[k];
+        mx = s > mx ? s : mx;
+      }
+    }
+  }
+  // block reduction (sum, max, or) via the scan's totals
+  long long tot[kQ];
+  block_exclusive_scan<kQ>(acc, tot);
+  __shared__ long long smx, sbad;
+  if (threadIdx.x == 0) smx = 0, sbad = 0;
+  __syncthreads();
+  if (mx) atomicMax(reinterpret_cast<unsigned long long*>(&smx), static_cast<unsigned long long>(mx));
+  if (bad) sbad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long* p = partials + static_cast<long long>(blockIdx.x) * kPartial;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) p[k] = tot[k];
+    p[6] = smx;
+    p[7] = sbad;
+  }
+}
+
+// One CTA: exclusive scan of the per-CTA sums (in place: partials[b][0..5]
+// become CTA offsets) and the totals: {T, N_c, N_b, fused tiles, split tiles,
+// pieces, max length, invalid flag}.  Also writes entry [n] of the offset
+// arrays.
+__global__ void __launch_bounds__(kScanThreads) k_plan_scan_partials(long long* __restrict__ partials, int nblk,
+                                                                     int32_t n, long long* __restrict__ totals,
+                                                                     int32_t* cu, int32_t* co, int64_t* bo,
+                                                                     int64_t* tof, int64_t* tos, int32_t* po) {
+  long long carry[kQ] = {0, 0, 0, 0, 0, 0};
+  __shared__ long long smx, sbad;
+  if (threadIdx.x == 0) smx = 0, sbad = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < nblk; b0 += kScanThreads) {
+    const int b = b0 + threadIdx.x;
+    long long x[kQ], tot[kQ];
+    long long* p = partials + static_cast<long long>(b) * kPartial;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) x[k] = b < nblk ? p[k] : 0;
+    if (b < nblk) {
+      if (p[6]) atomicMax(reinterpret_cast<unsigned long long*>(&smx), static_cast<unsigned long long>(p[6]));
+      if (p[7]) sbad = 1;
+    }
+    block_exclusive_scan<kQ>(x, tot);
+    if (b < nblk) {
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) p[k] = carry[k] + x[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) carry[k] += tot[k];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) totals[k] = carry[k];
+    totals[6] = smx;
+    totals[7] = sbad;
+    cu[n] = static_cast<int32_t>(carry[0]);
+    co[n] = static_cast<int32_t>(carry[1]);
+    bo[n] = carry[2];
+    tof[n] = carry[3];
+    tos[n] = carry[4];
+    po[n] = static_cast<int32_t>(carry[5]);
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_plan_scan_write(const int32_t* __restrict__ lengths, int32_t n,
+                                                                  int32_t C, int split_ok,
+                                                                  const long long* __restrict__ partials,
+                                                                  int32_t* __restrict__ cu, int32_t* __restrict__ co,
+                                                                  int64_t* __restrict__ bo, int64_t* __restrict__ tof,
+                                                                  int64_t* __restrict__ tos, int32_t* __restrict__ po) {
+  __shared__ int32_t s_len[kScanTile];
+  const long long base = static_cast<long long>(blockIdx.x) * kScanTile;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    const long long i = base + j * kScanThreads + threadIdx.x;
+    s_len[j * kScanThreads + threadIdx.x] = i < n ? lengths[i] : 0;
+  }
+  __syncthreads();
+  // thread t owns documents base + t*8 .. base + t*8 + 7
+  long long sum[kQ] = {0, 0, 0, 0, 0, 0}, tot[kQ];
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    const int32_t s = s_len[threadIdx.x * kScanItems + j];
+    if (s >= 1) {
+      long long q[kQ];
+      doc_quantities(s, C, split_ok != 0, q);
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) sum[k] += q[k];
+    }
+  }
+  block_exclusive_scan<kQ>(sum, tot);
+  const long long* p = partials + static_cast<long long>(blockIdx.x) * kPartial;
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) sum[k] += p[k];
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    const long long i = base + threadIdx.x * kScanItems + j;
+    if (i < n) {
+      cu[i] = static_cast<int32_t>(sum[0]);
+      co[i] = static_cast<int32_t>(sum[1]);
+      bo[i] = sum[2];
+      tof[i] = sum[3];
+      tos[i] = sum[4];
+      po[i] = static_cast<int32_t>(sum[5]);
+      const int32_t s = s_len[threadIdx.x * kScanItems + j];
+      if (s >= 1) {
+        long long q[kQ];
+        doc_quantities(s, C, split_ok != 0, q);
+#pragma unroll
+        for (int k = 0; k < kQ; ++k) sum[k] += q[k];
+      }
+    }
+  }
+}
+
+// Largest i in [0, n) with off[i] <= x (off ascending, off[0] = 0 <= x).
+template <typename T>
+__device__ __forceinline__ int32_t upper_doc(const T* __restrict__ off, int32_t n, long long x) {
+  int32_t lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (static_cast<long long>(off[mid]) <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Chunk table, causal pairs per chunk, and the shard of every full chunk
+// (full chunks take shard ids in chunk order: chunk c of document i is
+// preceded by po[i] sub-capacity pieces).
+__global__ void k_fill_chunks(int32_t n, int32_t C, long long nc, const int32_t* __restrict__ cu,
+                              const int32_t* __restrict__ co, const int32_t* __restrict__ po,
+                              int32_t* __restrict__ chunk_table, int64_t* __restrict__ chunk_pairs,
+                              int32_t* __restrict__ shard_of_chunk) {
+  for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < nc;
+       c += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int32_t doc = upper_doc(co, n, c);
+    const long long idx = c - co[doc];
+    const long long s = cu[doc + 1] - cu[doc];
+    const long long a = idx * C;
+    const long long len = s - a < C ? s - a : C;
+    const long long b = a + len;
+    int4 row;
+    row.x = doc;
+    row.y = static_cast<int32_t>(idx);
+    row.z = static_cast<int32_t>(cu[doc] + a);
+    row.w = static_cast<int32_t>(len);
+    reinterpret_cast<int4*>(chunk_table)[c] = row;
+    chunk_pairs[c] = (b * (b + 1) - a * (a + 1)) / 2;
+    if (shard_of_chunk && len == C) shard_of_chunk[c] = static_cast<int32_t>(c - po[doc]);
+  }
+}
+
+// qc = largest q with q(q+1)/2 <= local.
+__device__ __forceinline__ long long tri_root(long long local) {
+  long long q = static_cast<long long>((sqrt(8.0 * static_cast<double>(local) + 1.0) - 1.0) * 0.5);
+  while (q > 0 && q * (q + 1) / 2 > local) --q;
+  while ((q + 1) * (q + 2) / 2 <= local) ++q;
+  return q;
+}
+
+__global__ void k_fill_blocks(int32_t n, long long nb, const int32_t* __restrict__ co,
+                              const int64_t* __restrict__ bo, int32_t* __restrict__ block_table) {
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nb;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int32_t doc = upper_doc(bo, n, b);
+    const long long local = b - bo[doc];
+    const long long qc = tri_root(local);
+    const long long kc = local - qc * (qc + 1) / 2;
+    int2 row;
+    row.x = static_cast<int32_t>(co[doc] + qc);
+    row.y = static_cast<int32_t>(co[doc] + kc);
+    reinterpret_cast<int2*>(block_table)[b] = row;
+  }
+}
+
+__device__ __forceinline__ unsigned long long tile_key(long long weight, long long idx) {
+  return (static_cast<unsigned long long>(kWeightCap - weight) << kIdxBits) | static_cast<unsigned long long>(idx);
+}
+
+__device__ __forceinline__ void store_tile(int32_t* out, long long t, int32_t q0, int32_t qrows, int32_t kv0,
+                                           int32_t kvlen, int32_t blk, int32_t row_off, int32_t w) {
+  int4* o = reinterpret_cast<int4*>(out + t * 8);
+  o[0] = make_int4(q0, qrows, kv0, kvlen);
+  o[1] = make_int4(blk, row_off, w, 0);
+}
+
+// One row per document query tile: keys are the document's causal prefix.
+__global__ void k_fill_tiles_fused(int32_t n, long long ntiles, const int32_t* __restrict__ cu,
+                                   const int64_t* __restrict__ tof, int32_t* __restrict__ rows,
+                                   unsigned long long* __restrict__ keys) {
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < ntiles;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int32_t doc = upper_doc(tof, n, t);
+    const long long qt = t - tof[doc];
+    const long long s = cu[doc + 1] - cu[doc];
+    const long long qrows = s - qt * kTile < kTile ? s - qt * kTile : kTile;
+    const long long kvlen = qt * kTile + qrows;
+    const long long w = qt + 1;
+    store_tile(rows, t, static_cast<int32_t>(cu[doc] + qt * kTile), static_cast<int32_t>(qrows), cu[doc],
+               static_cast<int32_t>(kvlen), -1, static_cast<int32_t>(qt * kTile), static_cast<int32_t>(w));
+    keys[t] = tile_key(w, t);
+  }
+}
+
+// One row per query tile of every causal block (qc, kc); rows of a document
+// are ordered by block (qc, kc ascending), then query tile.  Needs C % 128 == 0.
+__global__ void k_fill_tiles_split(int32_t n, int32_t C, long long ntiles, const int32_t* __restrict__ cu,
+                                   const int64_t* __restrict__ bo, const int64_t* __restrict__ tos,
+                                   int32_t* __restrict__ rows, unsigned long long* __restrict__ keys) {
+  const long long tpc = C / kTile;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < ntiles;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int32_t doc = upper_doc(tos, n, t);
+    const long long local = t - tos[doc];
+    const long long s = cu[doc + 1] - cu[doc];
+    const long long nch = (s + C - 1) / C;
+    const long long last = s - (nch - 1) * C;
+    const long long tl = (last + kTile - 1) / kTile;
+    const long long full_rows = tpc * ((nch - 1) * nch / 2);
+    long long qc, kc, qt, blk_local;
+    if (local < full_rows) {
+      blk_local = local / tpc;
+      qt = local % tpc;
+      qc = tri_root(blk_local);
+      kc = blk_local - qc * (qc + 1) / 2;
+    } else {
+      const long long r = local - full_rows;
+      kc = r / tl;
+      qt = r % tl;
+      qc = nch - 1;
+      blk_local = (nch - 1) * nch / 2 + kc;
+    }
+    const long long qlen = qc == nch - 1 ? last : C;
+    const long long qrows = qlen - qt * kTile < kTile ? qlen - qt * kTile : kTile;
+    const long long kvlen = kc == qc ? qt * kTile + qrows : C;
+    const long long w = (kvlen + kTile - 1) / kTile;
+    store_tile(rows, t, static_cast<int32_t>(cu[doc] + qc * C + qt * kTile), static_cast<int32_t>(qrows),
+               static_cast<int32_t>(cu[doc] + kc * C), static_cast<int32_t>(kvlen),
+               static_cast<int32_t>(bo[doc] + blk_local), static_cast<int32_t>(qt * kTile),
+               static_cast<int32_t>(w));
+    keys[t] = tile_key(w, t);
+  }
+}
+
+__global__ void k_fill_pad(unsigned long long* keys, long long from, long long to) {
+  for (long long i = from + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < to;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    keys[i] = ~0ull;
+}
+
+// ---------------------------------------------------------------- bitonic sort
+constexpr int kSortTile = 4096;
+constexpr int kSortThreads = 1024;
+
+__device__ __forceinline__ void cmp_swap(unsigned long long& a, unsigned long long& b, bool ascending) {
+  if ((a > b) == ascending) {
+    const unsigned long long t = a;
+    a = b;
+    b = t;
+  }
+}
+
+// Sorts each kSortTile segment for every stage k <= kSortTile (direction by
+// the global index), i.e. the first log2(kSortTile) merge levels.
+__global__ void __launch_bounds__(kSortThreads) k_bitonic_local(unsigned long long* keys, long long n2) {
+  __shared__ unsigned long long s[kSortTile];
+  const long long base = static_cast<long long>(blockIdx.x) * kSortTile;
+  const int len = static_cast<int>(n2 - base < kSortTile ? n2 - base : kSortTile);
+  for (int i = threadIdx.x; i < len; i += kSortThreads) s[i] = keys[base + i];
+  __syncthreads();
+  for (int k = 2; k <= len; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < len / 2; i += kSortThreads) {
+        const int lo = (i / j) * 2 * j + (i % j);
+        const int hi = lo + j;
+        const bool asc = ((base + lo) & k) == 0;
+        cmp_swap(s[lo], s[hi], asc);
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < len; i += kSortThreads) keys[base + i] = s[i];
+}
+
+// One compare-exchange level with distance j >= kSortTile/2 of merge stage k.
+__global__ void k_bitonic_global(unsigned long long* keys, long long n2, long long k, long long j) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n2 / 2;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long lo = (i / j) * 2 * j + (i % j);
+    const long long hi = lo + j;
+    const bool asc = (lo & k) == 0;
+    unsigned long long a = keys[lo], b = keys[hi];
+    if ((a > b) == asc) {
+      keys[lo] = b;
+      keys[hi] = a;
+    }
+  }
+}
+
+// The remaining levels j < kSortTile/2 of merge stage k, inside one tile.
+__global__ void __launch_bounds__(kSortThreads) k_bitonic_tail(unsigned long long* keys, long long k) {
+  __shared__ unsigned long long s[kSortTile];
+  const long long base = static_cast<long long>(blockIdx.x) * kSortTile;
+  for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) s[i] = keys[base + i];
+  __syncthreads();
+  for (int j = kSortTile / 2; j > 0; j >>= 1) {
+    for (int i = threadIdx.x; i < kSortTile / 2; i += kSortThreads) {
+      const int lo = (i / j) * 2 * j + (i % j);
+      const int hi = lo + j;
+      const bool asc = ((base + lo) & k) == 0;
+      cmp_swap(s[lo], s[hi], asc);
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) keys[base + i] = s[i];
+}
+
+__global__ void k_gather_rows(const unsigned long long* __restrict__ keys, long long count,
+                              const int32_t* __restrict__ rows, int32_t* __restrict__ out) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long src = static_cast<long long>(keys[i] & kIdxMask);
+    const int4* a = reinterpret_cast<const int4*>(rows + src * 8);
+    int4* b = reinterpret_cast<int4*>(out + i * 8);
+    b[0] = a[0];
+    b[1] = a[1];
+  }
+}
+
+// ---------------------------------------------------------------- best fit
+// Key of a sub-capacity piece: (C - len) << 32 | doc, so ascending order is
+// length descending, then document ascending.
+__global__ void k_piece_keys(int32_t n, int32_t C, const int32_t* __restrict__ cu, const int32_t* __restrict__ po,
+                             unsigned long long* __restrict__ keys) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (po[i + 1] != po[i]) {
+      const int32_t s = cu[i + 1] - cu[i];
+      const int32_t last = s % C;  // non-zero here
+      keys[po[i]] = (static_cast<unsigned long long>(C - last) << 32) | static_cast<unsigned long long>(i);
+    }
+  }
+}
+
+constexpr int kBfdThreads = 1024;
+
+// Best fit over the pieces in sorted order: each goes to the open piece shard
+// with the least remaining capacity that still fits (lowest id on ties), else
+// opens a new shard.  Piece shards are numbered after the full-chunk shards.
+__global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long long* __restrict__ keys,
+                                                           int32_t npieces, int32_t C, int32_t nfull,
+                                                           const int32_t* __restrict__ co,
+                                                           int32_t* __restrict__ remaining,
+                                                           int32_t* __restrict__ shard_of_chunk,
+                                                           int32_t* __restrict__ num_shards) {
+  __shared__ unsigned long long wbest[kBfdThreads / 32];
+  __shared__ int32_t s_open;
+  if (threadIdx.x == 0) s_open = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int32_t p = 0; p < npieces; ++p) {
+    const unsigned long long key = keys[p];
+    const int32_t len = C - static_cast<int32_t>(key >> 32);
+    const int32_t doc = static_cast<int32_t>(key & 0xffffffffu);
+    const int32_t open = s_open;
+    unsigned long long best = ~0ull;
+    for (int32_t s = threadIdx.x; s < open; s += kBfdThreads) {
+      const int32_t r = remaining[s];
+      if (r >= len) {
+        const unsigned long long cand = (static_cast<unsigned long long>(r) << 32) | static_cast<unsigned>(s);
+        best = cand < best ? cand : best;
+      }
+    }
+    if (open > 32) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, off);
+        best = y < best ? y : best;
+      }
+      if (lane == 0) wbest[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        best = wbest[lane];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, off);
+          best = y < best ? y : best;
+        }
+      }
+    } else if (warp == 0) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, off);
+        best = y < best ? y : best;
+      }
+    }
+    if (threadIdx.x == 0) {
+      int32_t sid;
+      if (best == ~0ull) {
+        sid = s_open;
+        remaining[sid] = C - len;
+        s_open = sid + 1;
+      } else {
+        sid = static_cast<int32_t>(best & 0xffffffffu);
+        remaining[sid] -= len;
+      }
+      shard_of_chunk[co[doc + 1] - 1] = nfull + sid;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *num_shards = nfull + s_open;
+}
+
+// ---------------------------------------------------------------- FLOPs
+__global__ void k_flops_zero(int64_t* out, int32_t ns) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += gridDim.x * blockDim.x) out[i] = 0;
+}
+__global__ void k_flops_accum(const int64_t* __restrict__ pairs, const int32_t* __restrict__ shard, long long nc,
+                              long long per_pair, int64_t* out) {
+  for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < nc;
+       c += static_cast<long long>(gridDim.x) * blockDim.x) {
+    atomicAdd(reinterpret_cast<unsigned long long*>(out + shard[c]),
+              static_cast<unsigned long long>(pairs[c] * per_pair));
+  }
+}
+
+// ---------------------------------------------------------------- host helpers
+int grid_for(long long items, int threads, int cap = 1 << 16) {
+  long long g = (items + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+long long next_pow2(long long x) {
+  long long p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Sort n keys in place (buffer holds next_pow2(max(n, 1)) entries, padded
+// here with ~0).
+cudaError_t sort_keys(unsigned long long* keys, long long n, cudaStream_t st) {
+  const long long n2 = next_pow2(n < 2 ? 2 : n);
+  if (n2 > n) k_fill_pad<<<grid_for(n2 - n, 256), 256, 0, st>>>(keys, n, n2);
+  const long long tiles = (n2 + kSortTile - 1) / kSortTile;
+  k_bitonic_local<<<static_cast<unsigned>(tiles), kSortThreads, 0, st>>>(keys, n2);
+  for (long long k = 2LL * kSortTile; k <= n2; k <<= 1) {
+    for (long long j = k >> 1; j >= kSortTile; j >>= 1)
+      k_bitonic_global<<<grid_for(n2 / 2, 256), 256, 0, st>>>(keys, n2, k, j);
+    k_bitonic_tail<<<static_cast<unsigned>(n2 / kSortTile), kSortThreads, 0, st>>>(keys, k);
+  }
+  return cudaGetLastError();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace hdp
+
+using namespace hdp;
+
+extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num_docs, int32_t capacity,
+                                           uint32_t flags, void* stream, hdp_plan_t* out) {
+  if (!out) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: out is NULL");
+  *out = nullptr;
+  if (!d_lengths) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: d_lengths is NULL");
+  if (num_docs < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: num_docs must be >= 1");
+  if (capacity < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: capacity must be >= 1");
+  if (flags & ~HDP_PLAN_NO_SHARDS) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: unknown flags");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool split_ok = capacity % kTile == 0;
+  const int32_t n = num_docs;
+  const int nblk = static_cast<int>((static_cast<long long>(n) + kScanTile - 1) / kScanTile);
+
+  // ---- phase 1: per-document offsets (sizes known from n)
+  size_t off = 0;
+  const size_t o_cu = off; off = align256(off + sizeof(int32_t) * (n + 1));
+  const size_t o_co = off; off = align256(off + sizeof(int32_t) * (n + 1));
+  const size_t o_bo = off; off = align256(off + sizeof(int64_t) * (n + 1));
+  const size_t o_tof = off; off = align256(off + sizeof(int64_t) * (n + 1));
+  const size_t o_tos = off; off = align256(off + sizeof(int64_t) * (n + 1));
+  const size_t bytes1 = off;
+  const size_t o_po = 0;  // scratch: piece offsets, CTA partials, totals
+  size_t soff = align256(sizeof(int32_t) * (n + 1));
+  const size_t o_part = soff; soff = align256(soff + sizeof(long long) * kPartial * nblk);
+  const size_t o_tot = soff; soff = align256(soff + sizeof(long long) * kPartial);
+  const size_t sbytes = soff;
+
+  auto* plan = new (std::nothrow) hdp_plan_s;
+  if (!plan) return fail(HDP_ERR_OUT_OF_MEMORY, "hdp_plan_create: host allocation failed");
+  HDP_CUDA_TRY(cudaGetDevice(&plan->device));
+  plan->stream = st;
+  plan->flags = flags;
+  char* scratch = nullptr;
+  char* mem1 = nullptr;
+  auto cleanup = [&](hdp_status_t s) {
+    if (scratch) cudaFreeAsync(scratch, st);
+    if (mem1) cudaFreeAsync(mem1, st);
+    if (plan->mem) cudaFreeAsync(plan->mem, st);
+    delete plan;
+    return s;
+  };
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&mem1), bytes1, st);
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan offsets)"));
+  e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), sbytes, st);
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan scratch)"));
+  int32_t* cu = reinterpret_cast<int32_t*>(mem1 + o_cu);
+  int32_t* co = reinterpret_cast<int32_t*>(mem1 + o_co);
+  int64_t* bo = reinterpret_cast<int64_t*>(mem1 + o_bo);
+  int64_t* tof = reinterpret_cast<int64_t*>(mem1 + o_tof);
+  int64_t* tos = reinterpret_cast<int64_t*>(mem1 + o_tos);
+  int32_t* po = reinterpret_cast<int32_t*>(scratch + o_po);
+  long long* partials = reinterpret_cast<long long*>(scratch + o_part);
+  long long* totals = reinterpret_cast<long long*>(scratch + o_tot);
+
+  k_plan_reduce<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials);
+  k_plan_scan_partials<<<1, kScanThreads, 0, st>>>(partials, nblk, n, totals, cu, co, bo, tof, tos, po);
+  k_plan_scan_write<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials, cu, co, bo, tof,
+                                                   tos, po);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "plan scan launch"));
+  long long h_tot[kPartial];
+  e = cudaMemcpyAsync(h_tot, totals, sizeof h_tot, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "plan totals readback"));
+
+  const long long T = h_tot[0], nc = h_tot[1], nb = h_tot[2], ntf = h_tot[3], nts = h_tot[4], npc = h_tot[5];
+  if (h_tot[7]) return cleanup(fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: every length must be >= 1"));
+  if (T >= (1ll << 31))
+    return cleanup(fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: total tokens must be < 2^31"));
+  if (nb >= (1ll << 31) || nts >= (1ll << 31))
+    return cleanup(fail(HDP_ERR_UNSUPPORTED, "hdp_plan_create: more than 2^31 causal blocks or split tiles"));
+  const bool shards = !(flags & HDP_PLAN_NO_SHARDS);
+  if (shards && npc > kMaxPieces)
+    return cleanup(fail(HDP_ERR_UNSUPPORTED,
+                        "hdp_plan_create: more than 65536 sub-capacity pieces for best-fit packing "
+                        "(use HDP_PLAN_NO_SHARDS)"));
+
+  // ---- phase 2: tables sized by the totals
+  off = 0;
+  const size_t o_ct = off; off = align256(off + sizeof(int32_t) * 4 * nc);
+  const size_t o_bt = off; off = align256(off + sizeof(int32_t) * 2 * nb);
+  const size_t o_cp = off; off = align256(off + sizeof(int64_t) * nc);
+  const size_t o_sc = off; off = align256(off + (shards ? sizeof(int32_t) * nc : 0));
+  const size_t o_tf = off; off = align256(off + sizeof(int32_t) * 8 * ntf);
+  const size_t o_ts = off; off = align256(off + sizeof(int32_t) * 8 * nts);
+  const size_t o_ns = off; off = align256(off + sizeof(int32_t));
+  const size_t bytes2 = off;
+  e = cudaMallocAsync(&plan->mem, bytes2, st);
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan tables)"));
+  char* m2 = static_cast<char*>(plan->mem);
+  int32_t* chunk_table = reinterpret_cast<int32_t*>(m2 + o_ct);
+  int32_t* block_table = reinterpret_cast<int32_t*>(m2 + o_bt);
+  int64_t* chunk_pairs = reinterpret_cast<int64_t*>(m2 + o_cp);
+  int32_t* shard_of_chunk = shards ? reinterpret_cast<int32_t*>(m2 + o_sc) : nullptr;
+  int32_t* tiles_f = reinterpret_cast<int32_t*>(m2 + o_tf);
+  int32_t* tiles_s = split_ok ? reinterpret_cast<int32_t*>(m2 + o_ts) : nullptr;
+  int32_t* d_ns = reinterpret_cast<int32_t*>(m2 + o_ns);
+
+  // sort scratch: keys (power of two) + unsorted rows
+  const long long sort_n = std::max({ntf, split_ok ? nts : 0ll, shards ? npc : 0ll, 2ll});
+  const long long n2 = next_pow2(sort_n);
+  const long long nrows = std::max(ntf, split_ok ? nts : 0ll);
+  char* sort_mem = nullptr;
+  const size_t o_keys = 0;
+  size_t so = align256(sizeof(unsigned long long) * n2);
+  const size_t o_rows = so; so = align256(so + sizeof(int32_t) * 8 * nrows);
+  const size_t o_rem = so; so = align256(so + sizeof(int32_t) * (npc > 0 ? npc : 1));
+  e = cudaMallocAsync(reinterpret_cast<void**>(&sort_mem), so, st);
+  if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan sort scratch)"));
+  auto* keys = reinterpret_cast<unsigned long long*>(sort_mem + o_keys);
+  auto* rows = reinterpret_cast<int32_t*>(sort_mem + o_rows);
+  auto* rem = reinterpret_cast<int32_t*>(sort_mem + o_rem);
+  auto cleanup2 = [&](hdp_status_t s) {
+    cudaFreeAsync(sort_mem, st);
+    return cleanup(s);
+  };
+
+  if (nc > 0)
+    k_fill_chunks<<<grid_for(nc, 256), 256, 0, st>>>(n, capacity, nc, cu, co, po, chunk_table, chunk_pairs,
+                                                     shard_of_chunk);
+  if (nb > 0) k_fill_blocks<<<grid_for(nb, 256), 256, 0, st>>>(n, nb, co, bo, block_table);
+  // fused work list
+  k_fill_tiles_fused<<<grid_for(ntf, 256), 256, 0, st>>>(n, ntf, cu, tof, rows, keys);
+  e = sort_keys(keys, ntf, st);
+  if (e != cudaSuccess) return cleanup2(fail_cuda(e, "work list sort"));
+  k_gather_rows<<<grid_for(ntf, 256), 256, 0, st>>>(keys, ntf, rows, tiles_f);
+  // split work list
+  if (split_ok && nts > 0) {
+    k_fill_tiles_split<<<grid_for(nts, 256), 256, 0, st>>>(n, capacity, nts, cu, bo, tos, rows, keys);
+    e = sort_keys(keys, nts, st);
+    if (e != cudaSuccess) return cleanup2(fail_cuda(e, "split work list sort"));
+    k_gather_rows<<<grid_for(nts, 256), 256, 0, st>>>(keys, nts, rows, tiles_s);
+  }
+  int32_t h_ns = 0;
+  if (shards) {
+    if (npc > 0) {
+      k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, cu, po, keys);
+      e = sort_keys(keys, npc, st);
+      if (e != cudaSuccess) return cleanup2(fail_cuda(e, "piece sort"));
+    }
+    k_shard_bfd<<<1, kBfdThreads, 0, st>>>(keys, static_cast<int32_t>(npc), capacity,
+                                           static_cast<int32_t>(nc - npc), co, rem, shard_of_chunk, d_ns);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_ns, d_ns, sizeof h_ns, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cleanup2(fail_cuda(e, "shard packing"));
+  } else {
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cleanup2(fail_cuda(e, "plan table launch"));
+  }
+  cudaFreeAsync(sort_mem, st);
+  cudaFreeAsync(scratch, st);
+
+  // keep the phase-1 offsets: move them into the plan by keeping mem1 alive
+  plan->v.num_docs = n;
+  plan->v.capacity = capacity;
+  plan->v.num_chunks = static_cast<int32_t>(nc);
+  plan->v.num_shards = h_ns;
+  plan->v.num_blocks = nb;
+  plan->v.total_tokens = T;
+  plan->v.max_doc_len = static_cast<int32_t>(h_tot[6]);
+  plan->v.tile = kTile;
+  plan->v.cu_seqlens = cu;
+  plan->v.chunk_offsets = co;
+  plan->v.block_offsets = bo;
+  plan->v.chunk_table = chunk_table;
+  plan->v.block_table = block_table;
+  plan->v.chunk_pairs = chunk_pairs;
+  plan->v.shard_of_chunk = shard_of_chunk;
+  plan->v.tiles_fused = tiles_f;
+  plan->v.num_tiles_fused = ntf;
+  plan->v.tiles_split = tiles_s;
+  plan->v.num_tiles_split = split_ok ? nts : 0;
+  plan->tile_offsets_fused = tof;
+  plan->tile_offsets_split = tos;
+  plan->mem1 = mem1;
+  *out = plan;
+  return HDP_OK;
+}
+
+extern "C" hdp_status_t hdp_plan_create(const int32_t* d_lengths, int32_t num_docs, int32_t capacity, void* stream,
+                                        hdp_plan_t* out) {
+  return hdp_plan_create_ex(d_lengths, num_docs, capacity, HDP_PLAN_DEFAULT, stream, out);
+}
+
+extern "C" hdp_status_t hdp_plan_view(hdp_plan_t plan, hdp_plan_view_t* view) {
+  if (!plan || !view) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_view: NULL argument");
+  *view = plan->v;
+  return HDP_OK;
+}
+
+extern "C" hdp_status_t hdp_plan_destroy(hdp_plan_t plan) {
+  if (!plan) return HDP_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != plan->device) cudaSetDevice(plan->device);
+  cudaError_t e1 = plan->mem ? cudaFreeAsync(plan->mem, plan->stream) : cudaSuccess;
+  cudaError_t e2 = plan->mem1 ? cudaFreeAsync(plan->mem1, plan->stream) : cudaSuccess;
+  if (cur != plan->device) cudaSetDevice(cur);
+  delete plan;
+  if (e1 != cudaSuccess) return fail_cuda(e1, "hdp_plan_destroy");
+  if (e2 != cudaSuccess) return fail_cuda(e2, "hdp_plan_destroy");
+  return HDP_OK;
+}
+
+extern "C" hdp_status_t hdp_flops_per_shard(hdp_plan_t plan, int32_t d, int32_t hq, int64_t* d_out, void* stream) {
+  if (!plan || !d_out) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_flops_per_shard: NULL argument");
+  if (d < 1 || hq < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_flops_per_shard: d and hq must be >= 1");
+  if (!plan->v.shard_of_chunk)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_flops_per_shard: plan was created without shards");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t ns = plan->v.num_shards;
+  k_flops_zero<<<grid_for(ns, 256), 256, 0, st>>>(d_out, ns);
+  k_flops_accum<<<grid_for(plan->v.num_chunks, 256), 256, 0, st>>>(
+      plan->v.chunk_pairs, plan->v.shard_of_chunk, plan->v.num_chunks, 4ll * d * hq, d_out);
+  HDP_CUDA_TRY(cudaGetLastError());
+  return HDP_OK;
+}

@@ -1,0 +1,157 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Plan, shard packing, work lists and FLOPs must match bit for bit; attention
+must stay within max|dO| <= 1.5e-2, mean|dO| <= 1e-3, max|dLSE| <= 2e-3 on
+the same bf16-rounded inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import packed_varlen_attention_aware_gb300 as pkg
+from packed_varlen_attention_aware_gb300 import workloads as wl
+
+from parity_util import check_plan, full_parity, run_gpu, sample_rows, sampled_parity
+
+pytestmark = pytest.mark.gpu
+
+FUSED, SPLIT = pkg.HDP_MODE_FUSED, pkg.HDP_MODE_SPLIT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+# ---------------------------------------------------------------- plan (bit-exact)
+
+@pytest.mark.parametrize("name", ["tiny", "mb32k", "seq128k", "mix1m", "seq2m"])
+def test_plan_named_workloads(name):
+    w = wl.workload(name)
+    check_plan(list(w.lengths), w.capacity, d=w.d, hq=w.hq)
+
+
+def test_plan_figure2b():
+    ref = check_plan([32768, 16384, 8192, 4096, 4096], 8192)
+    assert ref["num_shards"] == 8
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_random(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 3000))
+    lengths = [int(x) for x in rng.integers(1, 5000, n)]
+    C = int(rng.choice([1, 7, 128, 256, 1000, 4096, 8192]))
+    if C == 1:
+        lengths = lengths[:50]
+    check_plan(lengths, C)
+
+
+def test_plan_many_docs_multi_cta_scan():
+    rng = np.random.default_rng(11)
+    lengths = [int(x) for x in rng.integers(1, 300, 20000)]  # > one scan tile of 2048 docs
+    check_plan(lengths, 256)
+    check_plan(lengths, 384, with_shards=False)
+
+
+def test_plan_rejects_bad_lengths():
+    dl = torch.tensor([5, 0, 3], dtype=torch.int32, device="cuda")
+    with pytest.raises(pkg.HdpError) as e:
+        pkg.hdp_plan_create(dl, 4)
+    assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------- attention, whole output
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_tiny(mode):
+    w = wl.workload("tiny")
+    full_parity(list(w.lengths), w.hq, w.hkv, w.d, w.capacity, mode)
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,C", [
+    ([1], 2, 1, 64, 128),
+    ([1, 2, 3, 127, 128, 129], 4, 2, 128, 128),
+    ([300, 1, 255, 513], 8, 2, 128, 256),
+    ([1000, 17, 640], 6, 2, 64, 384),     # group of 3: odd pair count
+    ([129, 257, 383], 3, 3, 128, 128),    # no GQA, odd head count
+    ([2048, 100, 1500, 33], 32, 8, 128, 512),
+])
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_small_cases(lengths, hq, hkv, d, C, mode):
+    full_parity(lengths, hq, hkv, d, C, mode, seed=len(lengths))
+
+
+def test_split_equals_fused():
+    lengths = [700, 1300, 5]
+    w = wl.Workload("c", tuple(lengths), 256, 8, 2, 128, 1.0, 3)
+    q, k, v = (t.cuda() for t in wl.qkv(w))
+    o1, l1, p1 = run_gpu(q, k, v, lengths, 256, FUSED)
+    o2, l2, p2 = run_gpu(q, k, v, lengths, 256, SPLIT)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1.6e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+def test_deterministic_and_packing_invariant():
+    hq, hkv, d = 8, 2, 128
+    docs = [300, 77, 1025]
+    data = [wl.qkv(wl.Workload("c", (s,), 512, hq, hkv, d, 1.0, 50 + i)) for i, s in enumerate(docs)]
+    alone = []
+    for (q, k, v), s in zip(data, docs):
+        o, lse, p = run_gpu(q.cuda(), k.cuda(), v.cuda(), [s], 512, FUSED)
+        alone.append((o.cpu(), lse.cpu()))
+    order = [2, 0, 1]
+    q = torch.cat([data[i][0] for i in order]).cuda()
+    k = torch.cat([data[i][1] for i in order]).cuda()
+    v = torch.cat([data[i][2] for i in order]).cuda()
+    lens = [docs[i] for i in order]
+    o, lse, p = run_gpu(q, k, v, lens, 512, FUSED)
+    o2, lse2, _ = run_gpu(q, k, v, lens, 512, FUSED, plan=p)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for j, i in enumerate(order):
+        assert torch.equal(o[cu[j]:cu[j + 1]].cpu(), alone[i][0])
+        assert torch.equal(lse[:, cu[j]:cu[j + 1]].cpu(), alone[i][1])
+
+
+def test_merge_rows_against_oracle():
+    g = torch.Generator().manual_seed(5)
+    m, rows, d = 5, 1000, 128
+    o_parts = torch.randn(m, rows, d, generator=g, dtype=torch.float64)
+    lse_parts = torch.randn(m, rows, generator=g, dtype=torch.float64) * 3
+    lse_parts[2, :100] = -float("inf")
+    lse_parts[:, 0] = -float("inf")
+    o_ref, lse_ref = oracle.merge(o_parts.numpy(), lse_parts.numpy())
+    o = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    pkg.hdp_lse_merge_rows(o_parts.float().cuda(), lse_parts.float().cuda(), o, lse)
+    torch.cuda.synchronize()
+    got_o = o.double().cpu().numpy()
+    got_l = lse.double().cpu().numpy()
+    assert got_l[0] == -np.inf and np.all(got_o[0] == 0)
+    assert np.max(np.abs(got_o[1:] - o_ref[1:])) <= 1.6e-2
+    assert np.max(np.abs(got_l[1:] - lse_ref[1:])) <= 1e-5
+
+
+# ---------------------------------------------------------------- named workloads, sampled rows
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mb32k_sampled(seed):
+    w = wl.workload("mb32k", seed)
+    q, k, v = (t.cuda() for t in wl.qkv(w, device="cpu"))
+    o, lse, plan = run_gpu(q, k, v, list(w.lengths), w.capacity, FUSED)
+    toks, heads = sample_rows(list(w.lengths), w.hq, 400, seed)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, f"mb32k seed {seed}")
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_seq128k_sampled(mode):
+    w = wl.workload("seq128k")
+    q, k, v = wl.qkv(w, device="cuda")
+    o, lse, plan = run_gpu(q, k, v, list(w.lengths), w.capacity, mode)
+    toks, heads = sample_rows(list(w.lengths), w.hq, 200, 7)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq128k mode {mode}")
