@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Throughput of the packed, document-masked, chunked causal attention path
+on GB300 ("ByteScale: Communication-Efficient Scaling of LLM Training with a
+2048K Context Length on 16384 GPUs", research digest, sections 2-3.2).
+
+One step = the whole hot path on one micro-batch resident in HBM:
+  plan (scans, chunk/block tables, best-fit shards, heaviest-first work list)
+  -> attention forward (FUSED: partials merged by the online softmax)
+  -> per-shard FLOPs.
+Metric: useful causal-attention TFLOP/s, 4*d*Hq*sum_i s_i(s_i+1)/2 per step,
+and its fraction of the bf16 dense tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mb32k]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "varlen causal attention fwd useful TFLOP/s and fraction of GB300 BF16 peak"
+L2_BYTES = 129 * 10**6
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_mb32k.md")
+ATTN_SRC = os.path.join(ROOT, "packed_varlen_attention_aware_gb300", "csrc", "attn_fwd.cu")
+
+
+def useful_flops(lengths, d, hq) -> int:
+    return sum(4 * d * hq * s * (s + 1) // 2 for s in lengths)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            out = {}
+            for key in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs"):
+                v = j.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                out[key] = float(v) if v is not None else FALLBACK_PEAKS[key]
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_from_profile():
+    """dram bytes per attention launch from the committed ncu summary, valid
+    only while the kernel source is the one that was profiled."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
+    sha, dram = None, None
+    for line in open(TRAFFIC_FILE):
+        if line.startswith("kernel_source_sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            dram = float(line.split(":", 1)[1].strip())
+    return dram if sha == want else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        rows = []
+        try:
+            for line in open(self.out.name):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_median": statistics.median(float(r[3]) for r in rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, q, k, v, seconds: float, seed: int):
+    """Time the fp64 oracle on a bounded sample of (token, head) rows of the
+    workload; returns (useful FLOPs of the sample, seconds, rows, threads)."""
+    import oracle
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    lengths = np.array(w.lengths, dtype=np.int64)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    rng = np.random.default_rng(seed)
+    doc_of = np.repeat(np.arange(len(lengths)), lengths)
+    kh, vh = wl.bf16_bits(k), wl.bf16_bits(v)
+    qh = np.zeros((T, w.hq, w.d), np.uint16)
+
+    def run(nrows):
+        toks = rng.integers(0, T, nrows)
+        heads = rng.integers(0, w.hq, nrows).astype(np.int32)
+        uniq = np.unique(toks)
+        import torch
+
+        qh[uniq] = wl.bf16_bits(q[torch.as_tensor(uniq, device=q.device)])
+        pos = toks - cu[doc_of[toks]]
+        flops = int(np.sum(4 * w.d * (pos + 1)))
+        t0 = time.perf_counter()
+        oracle.attention_rows(qh, kh, vh, cu, w.hq, w.hkv, w.d, w.scale, toks, heads)
+        return flops, time.perf_counter() - t0
+
+    f0, t0 = run(64)  # calibration
+    rate = f0 / max(t0, 1e-6)
+    n = max(64, int(64 * seconds * rate / max(f0, 1)))
+    f1, t1 = run(n)
+    return f1, t1, n, oracle.num_threads()
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def reference_arm(args, rank):
+    """The fp64 oracle as it stands, on the host cores, on our workload."""
+    if rank != 0:
+        return 0
+    import torch
+
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    w = wl.workload(args.workload, args.seed)
+    q, k, v = wl.qkv(w, device="cpu")
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step, args.seed + 1000)
+    flops, secs, rows = 0, 0.0, 0
+    threads = 1
+    for i in range(args.steps):
+        f, t, n, threads = oracle_sample(w, q, k, v, per_step, args.seed + i)
+        flops, secs, rows = flops + f, secs + t, rows + n
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args, "oracle"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} random (token, head) rows of {w.name} over {args.steps} steps, "
+                                   f"~{per_step:.1f} s each, fp64 C oracle with OpenMP on {cpu_model()}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, args, mode):
+    T = w.total_tokens
+    in_bytes = T * (w.hq + 2 * w.hkv) * w.d * 2
+    return {
+        "workload": f"{w.name}: {len(w.lengths)} documents packed into {T} tokens, Hq={w.hq}, Hkv={w.hkv}, "
+                    f"d={w.d}, capacity C={w.capacity}, seed {w.seed}",
+        "tokens": T, "documents": len(w.lengths), "max_doc": max(w.lengths), "hq": w.hq, "hkv": w.hkv, "d": w.d,
+        "capacity": w.capacity, "seed": w.seed, "mode": mode,
+        "useful_flops_per_step": useful_flops(w.lengths, w.d, w.hq),
+        "l2": f"inputs larger than L2: Q/K/V {in_bytes / 2**20:.0f} MiB vs 129 MB L2" if in_bytes > L2_BYTES
+        else f"L2 flushed between steps (inputs {in_bytes / 2**20:.1f} MiB)",
+    }
+
+
+# ---------------------------------------------------------------- our arm
+
+def our_arm(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import build as native_build
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    native_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = wl.workload(args.workload, args.seed + rank)
+    mode = pkg.HDP_MODE_SPLIT if args.mode == "split" else pkg.HDP_MODE_FUSED
+    q, k, v = wl.qkv(w, device=str(dev))
+    T = w.total_tokens
+    lengths_d = torch.tensor(w.lengths, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, T), dtype=torch.float32, device=dev)
+    flops_step = useful_flops(w.lengths, w.d, w.hq)
+    in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+    flush = None if in_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    probe = pkg.hdp_plan_create(lengths_d, w.capacity)
+    nshards = probe.view.num_shards
+    ws_bytes = pkg.hdp_attention_workspace_bytes(probe, w.hq, w.d, mode)
+    probe.destroy()
+    shard_flops = torch.empty(max(nshards, 1), dtype=torch.int64, device=dev)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    attn_events = []
+
+    def step(record=False):
+        plan = pkg.hdp_plan_create(lengths_d, w.capacity, stream=stream)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, mode, workspace, o, lse, stream=stream)
+        if record:
+            e1.record(stream)
+            attn_events.append((e0, e1))
+        pkg.hdp_flops_per_shard(plan, w.d, w.hq, shard_flops, stream=stream)
+        plan.destroy()
+        if flush is not None:
+            flush.zero_()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pkg.hdp_device_status()
+    assert int(shard_flops[:nshards].sum().item()) == flops_step, "per-shard FLOPs do not sum to the total"
+
+    launches0 = pkg.hdp_kernel_launch_count()
+    with ClockSampler(local) as clocks:
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+    launches = pkg.hdp_kernel_launch_count() - launches0
+    pkg.hdp_device_status()
+    ms = t0.elapsed_time(t1)
+    attn_ms = sum(a.elapsed_time(b) for a, b in attn_events) / len(attn_events)
+    clk = clocks.summary()
+
+    # ---- end to end through the public API with host buffers
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    lh = torch.tensor(w.lengths, dtype=torch.int32).pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    fh = torch.empty(shard_flops.shape, dtype=torch.int64).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ld = torch.empty_like(lengths_d)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        plan = pkg.hdp_plan_create(ld, w.capacity, stream=stream)
+        pkg.hdp_attention_fwd(plan, qd, kd, vd, w.hq, w.hkv, w.d, w.scale, mode, workspace, o, lse, stream=stream)
+        pkg.hdp_flops_per_shard(plan, w.d, w.hq, shard_flops, stream=stream)
+        oh.copy_(o, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+        fh.copy_(shard_flops, non_blocking=True)
+        plan.destroy()
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = in_bytes + lh.numel() * 4
+    d2h = oh.numel() * 2 + lseh.numel() * 4 + fh.numel() * 8
+
+    times = torch.tensor([ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
+    total_flops = torch.tensor([float(flops_step)], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+        dist.all_reduce(total_flops, op=dist.ReduceOp.SUM)
+    ms, e2e_ms, attn_ms_max = times.tolist()
+    job_flops = total_flops.item()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        f, secs, rows, threads = oracle_sample(w, q, k, v, args.cpu_seconds, args.seed + 7)
+        cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} random (token, head) rows of {w.name}, {secs:.1f} s, fp64 C oracle with "
+                         f"OpenMP on {cpu_model()}"}
+    if rank == 0:
+        peaks, src = load_peaks()
+        achieved = flops_step / (attn_ms * 1e-3) / 1e12
+        value = job_flops * args.steps / (ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, args, args.mode),
+            "frac_of_bf16_peak": value / (peaks["bf16_tflops"] * ws),
+            "roofline": {"bound": "tensor", "kernel": "k_attn_fwd", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{src} bf16 dense burst",
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "attn_ms": attn_ms, "traffic": traffic_from_profile()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": job_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mb32k", choices=["tiny", "mb32k", "seq128k", "mix1m", "seq2m"])
+    ap.add_argument("--mode", choices=["fused", "split"], default="fused")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, rank)
+    return our_arm(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -191,6 +191,10 @@ hdp_status_t hdp_device_status(void* stream);
 const char* hdp_status_string(hdp_status_t status);
 const char* hdp_last_error_message(void);
 
+/* Number of CUDA kernels this library has enqueued in this process (all
+ * devices, all threads).  Diagnostic counter; never reset. */
+uint64_t hdp_kernel_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,4 +22,5 @@ from .oracle import (  # noqa: F401
     flops_per_shard,
     tile_worklist,
     library_path,
+    num_threads,
 )

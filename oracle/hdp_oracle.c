@@ -24,6 +24,9 @@
  * the code that takes them.
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -38,6 +41,15 @@ static double bf16_to_double(uint16_t b) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* Threads the oracle's parallel loops use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }
 
 /* ------------------------------------------------------------------ plan */

@@ -49,6 +49,8 @@ def _load():
             lib.oracle_attention.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P]
             lib.oracle_attention_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P, P, P, i64, P, P]
             lib.oracle_merge.argtypes = [i32, i64, i32, P, P, P, P]
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -64,6 +66,11 @@ def _bits(x: np.ndarray) -> np.ndarray:
     if x.dtype != np.uint16:
         raise TypeError("pass bf16 data as uint16 bit patterns")
     return x
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().oracle_num_threads())
 
 
 def plan_sizes(lengths, C: int):

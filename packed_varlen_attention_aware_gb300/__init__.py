@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     hdp_attention_workspace_bytes,
     hdp_device_status,
     hdp_flops_per_shard,
+    hdp_kernel_launch_count,
     hdp_last_error_message,
     hdp_lse_merge,
     hdp_lse_merge_rows,

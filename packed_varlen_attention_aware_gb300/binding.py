@@ -29,6 +29,7 @@ EXPORTED = (
     "hdp_plan_create", "hdp_plan_create_ex", "hdp_plan_view", "hdp_plan_destroy",
     "hdp_attention_workspace_bytes", "hdp_attention_fwd", "hdp_lse_merge", "hdp_lse_merge_rows",
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
+    "hdp_kernel_launch_count",
 )
 
 
@@ -84,6 +85,8 @@ def load(path: str | None = None):
             f = getattr(lib, name)
             f.argtypes = args
             f.restype = ctypes.c_int
+        lib.hdp_kernel_launch_count.argtypes = []
+        lib.hdp_kernel_launch_count.restype = ctypes.c_uint64
         lib.hdp_status_string.restype = ctypes.c_char_p
         lib.hdp_last_error_message.restype = ctypes.c_char_p
         _lib = lib
@@ -225,6 +228,10 @@ def hdp_device_status(stream=None):
 
 def hdp_status_string(status: int) -> str:
     return load().hdp_status_string(status).decode()
+
+
+def hdp_kernel_launch_count() -> int:
+    return int(load().hdp_kernel_launch_count())
 
 
 def hdp_last_error_message() -> str:

@@ -1,6 +1,7 @@
 // Status strings, thread-local error messages and the device error word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -12,10 +13,13 @@ thread_local std::string g_last_error;
 __device__ unsigned int g_device_error;  // 0 = ok, else a code from the kernels
 
 std::mutex g_mu;
+std::atomic<unsigned long long> g_launches{0};
 unsigned int* g_err_ptr[64] = {nullptr};
 }  // namespace
 
 namespace hdp {
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 hdp_status_t fail(hdp_status_t st, const std::string& msg) {
   g_last_error = msg;
@@ -57,6 +61,8 @@ const char* hdp_status_string(hdp_status_t s) {
 }
 
 const char* hdp_last_error_message(void) { return g_last_error.c_str(); }
+
+uint64_t hdp_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 hdp_status_t hdp_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);

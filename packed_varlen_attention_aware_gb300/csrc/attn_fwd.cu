@@ -151,9 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.p_full[s], 4);  // one arrive per softmax warp
       mbar_init(&bars.o_full[s], 1);
-      mbar_init(&bars.o_empty[s], 128);
+      mbar_init(&bars.o_empty[s], 4);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
@@ -247,62 +247,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Issue order per key tile j: P.V of slot 0, then S = Q K^T of slot 0 for
+    // tile j+1, then the same for slot 1.  The softmax of one slot runs while
+    // the tensor core works on the other slot.  S(j+1) of a slot overwrites the
+    // TMEM columns that P(j) of the same slot occupies; the two MMAs are issued
+    // back to back by this thread and execute in issue order.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
       const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-      uint32_t q_uses[2] = {0, 0}, pv_count[2] = {0, 0}, units_done[2] = {0, 0};
+      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
       long long kuse = 0, vuse = 0;
       bool ok = true;
+      auto issue_qk = [&](int s, int kst) {
+        const uint32_t qa = sQ + s * L::kTileBytes;
+        const uint32_t kb = sK + kst * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          umma_ss(tS(s), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+        }
+        umma_commit(&bars.s_full[s]);
+      };
+      auto issue_pv = [&](int s, int vst, bool accumulate) {
+        const uint32_t vb = sV + vst * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tO(s), tS(s) + kk * 8, sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv,
+                  (accumulate || kk > 0) ? 1u : 0u);
+        umma_commit(&bars.o_full[s]);
+      };
       for (long long k = 0; ok; ++k) {
         const long long u = unit_index(k, cta, nctas);
         if (u >= total_units) break;
         const Unit x = load_unit(p, u);
         const int nslots = x.valid1 ? 2 : 1;
+        const int n = x.ntiles_kv;
         for (int s = 0; s < nslots && ok; ++s) {
           ok = mbar_wait(&bars.q_full[s], q_uses[s] & 1, abort_word, p.err, kErrQFull);
           ++q_uses[s];
         }
-        for (int j = 0; j < x.ntiles_kv && ok; ++j) {
-          const int kst = static_cast<int>(kuse % kStages);
-          ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
-          for (int s = 0; s < nslots && ok; ++s) {
-            // S_s aliases P_s of the previous P.V of this slot: wait for it
-            if (pv_count[s] > 0) ok = mbar_wait(&bars.o_full[s], (pv_count[s] - 1) & 1, abort_word, p.err, kErrOFull);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t qa = sQ + s * L::kTileBytes;
-            const uint32_t kb = sK + kst * L::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-              umma_ss(tS(s), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
-            }
-            umma_commit(&bars.s_full[s]);
-            if (j == x.ntiles_kv - 1) umma_commit(&bars.q_empty[s]);
-          }
-          if (!ok) break;
-          umma_commit(&bars.k_empty[kst]);
-          ++kuse;
+        // S(0) for both slots
+        int kst = static_cast<int>(kuse % kStages);
+        if (ok) ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
+        if (!ok) break;
+        tc_fence_after();
+        for (int s = 0; s < nslots; ++s) {
+          issue_qk(s, kst);
+          if (n == 1) umma_commit(&bars.q_empty[s]);
+        }
+        umma_commit(&bars.k_empty[kst]);
+        ++kuse;
+        for (int j = 0; j < n && ok; ++j) {
           const int vst = static_cast<int>(vuse % kStages);
           ok = mbar_wait(&bars.v_full[vst], (vuse / kStages) & 1, abort_word, p.err, kErrVFull);
+          const bool more = j + 1 < n;
+          kst = static_cast<int>(kuse % kStages);
           for (int s = 0; s < nslots && ok; ++s) {
             // P_s(j) written (and O_s rescaled) by the softmax warps
-            ok = mbar_wait(&bars.p_full[s], pv_count[s] & 1, abort_word, p.err, kErrPFull);
-            // first P.V of a unit overwrites O_s: the previous epilogue must have read it
+            ok = mbar_wait(&bars.p_full[s], p_uses[s] & 1, abort_word, p.err, kErrPFull);
+            ++p_uses[s];
+            // the first P.V of a unit overwrites O_s: the previous epilogue must have read it
             if (ok && j == 0 && units_done[s] > 0)
               ok = mbar_wait(&bars.o_empty[s], (units_done[s] - 1) & 1, abort_word, p.err, kErrOEmpty);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vb = sV + vst * L::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_ts(tO(s), tS(s) + kk * 8, sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars.o_full[s]);
-            ++pv_count[s];
+            issue_pv(s, vst, j > 0);
+            if (more) {
+              if (s == 0) {
+                ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_qk(s, kst);
+              if (j + 2 == n) umma_commit(&bars.q_empty[s]);
+            }
           }
           if (!ok) break;
+          if (more) {
+            umma_commit(&bars.k_empty[kst]);
+            ++kuse;
+          }
           umma_commit(&bars.v_empty[vst]);
           ++vuse;
         }
@@ -315,10 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int s = warp >> 2;              // slot
+    const int s = warp >> 2;                 // slot
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = tile row
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t s_count = 0, units_done = 0;
+    const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
+    uint32_t s_count = 0;
     bool ok = true;
     for (long long k = 0; ok; ++k) {
       const long long u = unit_index(k, cta, nctas);
@@ -347,11 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
         }
-        float mt = -INFINITY;
+        // row max: four independent chains of 3-input max
+        float mc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          mc[c] = __uint_as_float(r[c][0]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[c][i]));
+          for (int i = 1; i < 31; i += 2) mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+          mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+        }
+        const float mt = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
         const float mt_scaled = mt * p.scale_log2;
         bool rescale_o = false;
         float alpha = 1.f;
@@ -362,23 +393,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
           rescale_o = j > 0;
         }
-        const float neg_m = -m;
-        float rowsum = 0.f;
+        const uint64_t negm2 = pack_f32x2(-m, -m);
+        uint64_t acc[4];
         uint32_t pk[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          acc[c] = pack_f32x2(0.f, 0.f);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][i]), p.scale_log2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), p.scale_log2, neg_m));
-            rowsum += p0 + p1;
+            const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), scale2,
+                                          negm2);
+            const float p0 = ex2_approx(lo_f32(t));
+            const float p1 = ex2_approx(hi_f32(t));
+            acc[c] = fadd_f32x2(acc[c], pack_f32x2(p0, p1));
             pk[c >> 1][(c & 1) * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
-        l += rowsum;
-        tmem_st32(tS(s) + lane_off, pk[0]);
+          if (c == 1) tmem_st32(tS(s) + lane_off, pk[0]);
+        }
         tmem_st32(tS(s) + lane_off + 32, pk[1]);
+        const uint64_t a01 = fadd_f32x2(acc[0], acc[1]), a23 = fadd_f32x2(acc[2], acc[3]);
+        const uint64_t a = fadd_f32x2(a01, a23);
+        l += lo_f32(a) + hi_f32(a);
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // P.V of tile j-1 is complete: it finished before S_s(j) was computed
+          // P.V of tile j-1 is complete: S_s(j) was committed after it
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -391,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.p_full[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[s]);
       }
       if (!ok) break;
       // ---- epilogue: wait for the last P.V, normalize, store
@@ -441,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse_part[(static_cast<long long>(x.blk) * p.hq + h) * p.C + x.row_off + row] = lse_val;
       }
       tc_fence_before();
-      mbar_arrive(&bars.o_empty[s]);
-      ++units_done;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.o_empty[s]);
     }
   }
   tc_fence_before();
@@ -525,6 +563,7 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   const int smem = SmemLayout<D>::kBytes + 1024;
   HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   k_attn_fwd<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
+  note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   return HDP_OK;
 }

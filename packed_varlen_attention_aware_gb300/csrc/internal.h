@@ -25,6 +25,9 @@ hdp_status_t fail_cuda(cudaError_t e, const char* what);
 // consistency checks).  Defined in api.cu; read by hdp_device_status.
 unsigned int* device_error_word();
 
+// Count one kernel enqueued by this library (reported by hdp_kernel_launch_count).
+void note_launch();
+
 }  // namespace hdp
 
 struct hdp_plan_s {

@@ -157,6 +157,7 @@ hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, co
     k_merge_blocks<1><<<g, kMergeThreads, 0, st>>>(src, d, static_cast<__nv_bfloat16*>(o), lse);
   else
     k_merge_blocks<2><<<g, kMergeThreads, 0, st>>>(src, d, static_cast<__nv_bfloat16*>(o), lse);
+  note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   return HDP_OK;
 }
@@ -190,6 +191,7 @@ extern "C" hdp_status_t hdp_lse_merge_rows(int32_t m, int64_t rows, int32_t d, c
     k_merge_rows<1><<<g, kMergeThreads, 0, st>>>(src, d, static_cast<__nv_bfloat16*>(o), lse);
   else
     k_merge_rows<2><<<g, kMergeThreads, 0, st>>>(src, d, static_cast<__nv_bfloat16*>(o), lse);
+  note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   return HDP_OK;
 }

@@ -573,13 +573,20 @@ long long next_pow2(long long x) {
 // here with ~0).
 cudaError_t sort_keys(unsigned long long* keys, long long n, cudaStream_t st) {
   const long long n2 = next_pow2(n < 2 ? 2 : n);
-  if (n2 > n) k_fill_pad<<<grid_for(n2 - n, 256), 256, 0, st>>>(keys, n, n2);
+  if (n2 > n) {
+    k_fill_pad<<<grid_for(n2 - n, 256), 256, 0, st>>>(keys, n, n2);
+    note_launch();
+  }
   const long long tiles = (n2 + kSortTile - 1) / kSortTile;
   k_bitonic_local<<<static_cast<unsigned>(tiles), kSortThreads, 0, st>>>(keys, n2);
+  note_launch();
   for (long long k = 2LL * kSortTile; k <= n2; k <<= 1) {
-    for (long long j = k >> 1; j >= kSortTile; j >>= 1)
+    for (long long j = k >> 1; j >= kSortTile; j >>= 1) {
       k_bitonic_global<<<grid_for(n2 / 2, 256), 256, 0, st>>>(keys, n2, k, j);
+      note_launch();
+    }
     k_bitonic_tail<<<static_cast<unsigned>(n2 / kSortTile), kSortThreads, 0, st>>>(keys, k);
+    note_launch();
   }
   return cudaGetLastError();
 }
@@ -646,9 +653,12 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   long long* totals = reinterpret_cast<long long*>(scratch + o_tot);
 
   k_plan_reduce<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials);
+  note_launch();
   k_plan_scan_partials<<<1, kScanThreads, 0, st>>>(partials, nblk, n, totals, cu, co, bo, tof, tos, po);
+  note_launch();
   k_plan_scan_write<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials, cu, co, bo, tof,
                                                    tos, po);
+  note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "plan scan launch"));
   long long h_tot[kPartial];
@@ -708,31 +718,42 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
     return cleanup(s);
   };
 
-  if (nc > 0)
+  if (nc > 0) {
     k_fill_chunks<<<grid_for(nc, 256), 256, 0, st>>>(n, capacity, nc, cu, co, po, chunk_table, chunk_pairs,
                                                      shard_of_chunk);
-  if (nb > 0) k_fill_blocks<<<grid_for(nb, 256), 256, 0, st>>>(n, nb, co, bo, block_table);
+    note_launch();
+  }
+  if (nb > 0) {
+    k_fill_blocks<<<grid_for(nb, 256), 256, 0, st>>>(n, nb, co, bo, block_table);
+    note_launch();
+  }
   // fused work list
   k_fill_tiles_fused<<<grid_for(ntf, 256), 256, 0, st>>>(n, ntf, cu, tof, rows, keys);
+  note_launch();
   e = sort_keys(keys, ntf, st);
   if (e != cudaSuccess) return cleanup2(fail_cuda(e, "work list sort"));
   k_gather_rows<<<grid_for(ntf, 256), 256, 0, st>>>(keys, ntf, rows, tiles_f);
+  note_launch();
   // split work list
   if (split_ok && nts > 0) {
     k_fill_tiles_split<<<grid_for(nts, 256), 256, 0, st>>>(n, capacity, nts, cu, bo, tos, rows, keys);
+    note_launch();
     e = sort_keys(keys, nts, st);
     if (e != cudaSuccess) return cleanup2(fail_cuda(e, "split work list sort"));
     k_gather_rows<<<grid_for(nts, 256), 256, 0, st>>>(keys, nts, rows, tiles_s);
+    note_launch();
   }
   int32_t h_ns = 0;
   if (shards) {
     if (npc > 0) {
       k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, cu, po, keys);
+      note_launch();
       e = sort_keys(keys, npc, st);
       if (e != cudaSuccess) return cleanup2(fail_cuda(e, "piece sort"));
     }
     k_shard_bfd<<<1, kBfdThreads, 0, st>>>(keys, static_cast<int32_t>(npc), capacity,
                                            static_cast<int32_t>(nc - npc), co, rem, shard_of_chunk, d_ns);
+    note_launch();
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaMemcpyAsync(&h_ns, d_ns, sizeof h_ns, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -804,8 +825,10 @@ extern "C" hdp_status_t hdp_flops_per_shard(hdp_plan_t plan, int32_t d, int32_t 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int32_t ns = plan->v.num_shards;
   k_flops_zero<<<grid_for(ns, 256), 256, 0, st>>>(d_out, ns);
+  note_launch();
   k_flops_accum<<<grid_for(plan->v.num_chunks, 256), 256, 0, st>>>(
       plan->v.chunk_pairs, plan->v.shard_of_chunk, plan->v.num_chunks, 4ll * d * hq, d_out);
+  note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   return HDP_OK;
 }
