@@ -34,6 +34,9 @@ from .binding import (  # noqa: F401
     hdp_lse_merge,
     hdp_lse_merge_rows,
     hdp_plan_create,
+    hdp_plan_create_ex,
+    hdp_plan_destroy,
+    hdp_plan_view,
     hdp_status_string,
     load,
 )

@@ -192,6 +192,18 @@ def hdp_plan_create(d_lengths, capacity: int, flags: int = HDP_PLAN_DEFAULT, str
     return Plan(h)
 
 
+def hdp_plan_create_ex(d_lengths, capacity: int, flags: int, stream=None) -> Plan:
+    return hdp_plan_create(d_lengths, capacity, flags=flags, stream=stream)
+
+
+def hdp_plan_view(plan: Plan) -> PlanView:
+    return plan.view
+
+
+def hdp_plan_destroy(plan: Plan):
+    plan.destroy()
+
+
 def hdp_attention_workspace_bytes(plan: Plan, hq: int, d: int, mode: int) -> int:
     n = ctypes.c_size_t()
     _check(load().hdp_attention_workspace_bytes(plan.handle, hq, d, mode, ctypes.byref(n)),

@@ -628,3 +628,4 @@ extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const 
   if (r != HDP_OK || !split) return r;
   return launch_merge_blocks(plan, o_part, lse_part, hq, d, o, lse, st);
 }
+

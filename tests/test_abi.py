@@ -38,6 +38,11 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_python_binding_has_every_symbol():
+    for name in declared_symbols():
+        assert callable(getattr(pkg, name, None)), name
+
+
 def test_status_strings(lib):
     assert pkg.hdp_status_string(pkg.HDP_OK) == "HDP_OK"
     assert pkg.hdp_status_string(pkg.HDP_ERR_DEVICE_TIMEOUT) == "HDP_ERR_DEVICE_TIMEOUT"
