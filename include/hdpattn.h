@@ -152,6 +152,30 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
                                size_t workspace_bytes, void* o, float* lse, void* stream);
 
 /*
+ * SPLIT-mode attention that allocates nothing.  The paper has no counterpart;
+ * this entry exists for callers that cannot allocate device memory at the time
+ * they run attention: code running while a CUDA graph is being captured
+ * (cudaMalloc cannot be captured), servers that reserve all device memory up
+ * front and forbid allocation on the request path, and callers that must avoid
+ * the device-wide synchronisation cudaMalloc/cudaFree can imply.
+ * Same arguments and results as hdp_attention_fwd with mode HDP_MODE_SPLIT,
+ * but the partials live in a fixed 64 MiB scratch area inside the library
+ * (every GPU that loads the library reserves it until the process exits).
+ *   - Plans whose SPLIT workspace (hdp_attention_workspace_bytes) exceeds
+ *     64 MiB are rejected with HDP_ERR_INVALID_ARGUMENT and a message.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call on a device resolves the scratch area's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one scratch area and overwrites it; nothing in it
+ *     needs to start at zero.  Calls that overlap on the GPU (other streams,
+ *     other threads) race on it and must be serialised by the caller.
+ */
+hdp_status_t hdp_attention_fwd_split_noalloc(hdp_plan_t plan, const void* q, const void* k, const void* v,
+                                             int32_t hq, int32_t hkv, int32_t d, float scale, void* o, float* lse,
+                                             void* stream);
+
+/*
  * Exact log-sum-exp merge of the causal blocks of every query chunk
  * (section 3.2: the partial results of the ring steps are combined):
  *   M = max_k lse_k, lse = M + ln sum_k exp(lse_k - M), o = sum_k exp(lse_k - lse) o_k

@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     HdpError,
     Plan,
     hdp_attention_fwd,
+    hdp_attention_fwd_split_noalloc,
     hdp_attention_workspace_bytes,
     hdp_device_status,
     hdp_flops_per_shard,

@@ -29,7 +29,7 @@ EXPORTED = (
     "hdp_plan_create", "hdp_plan_create_ex", "hdp_plan_view", "hdp_plan_destroy",
     "hdp_attention_workspace_bytes", "hdp_attention_fwd", "hdp_lse_merge", "hdp_lse_merge_rows",
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
-    "hdp_kernel_launch_count",
+    "hdp_kernel_launch_count", "hdp_attention_fwd_split_noalloc",
 )
 
 
@@ -74,6 +74,7 @@ def load(path: str | None = None):
             "hdp_plan_destroy": [V],
             "hdp_attention_workspace_bytes": [V, I32, I32, I32, ctypes.POINTER(SZ)],
             "hdp_attention_fwd": [V, V, V, V, I32, I32, I32, F32, I32, V, SZ, V, V, V],
+            "hdp_attention_fwd_split_noalloc": [V, V, V, V, I32, I32, I32, F32, V, V, V],
             "hdp_lse_merge": [V, V, V, I32, I32, V, V, V],
             "hdp_lse_merge_rows": [I32, I64, I32, V, V, V, V, V],
             "hdp_flops_per_shard": [V, I32, I32, V, V],
@@ -217,6 +218,14 @@ def hdp_attention_fwd(plan: Plan, q, k, v, hq: int, hkv: int, d: int, scale: flo
     _check(load().hdp_attention_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), hq, hkv, d, float(scale), mode,
                                     _ptr(workspace), ws_bytes, _ptr(o), _ptr(lse), _stream(stream)),
            "hdp_attention_fwd")
+
+
+def hdp_attention_fwd_split_noalloc(plan: Plan, q, k, v, hq: int, hkv: int, d: int, scale: float, o, lse,
+                                    stream=None):
+    """SPLIT attention using the library's fixed scratch area (no allocation)."""
+    _check(load().hdp_attention_fwd_split_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), hq, hkv, d, float(scale),
+                                                  _ptr(o), _ptr(lse), _stream(stream)),
+           "hdp_attention_fwd_split_noalloc")
 
 
 def hdp_lse_merge(plan: Plan, o_part, lse_part, hq: int, d: int, o, lse, stream=None):

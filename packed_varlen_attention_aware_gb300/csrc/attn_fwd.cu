@@ -629,3 +629,61 @@ extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const 
   return launch_merge_blocks(plan, o_part, lse_part, hq, d, o, lse, st);
 }
 
+// ---------------------------------------------------------------- SPLIT without allocation
+// Some callers cannot allocate device memory when they run attention: code
+// that executes while a CUDA graph is being captured (cudaMalloc cannot be
+// captured), serving processes that reserve all device memory up front and
+// forbid allocation on the request path, and callers that must not take the
+// device-wide synchronisation cudaMalloc/cudaFree may imply.  For them SPLIT
+// mode can use a fixed scratch area that is part of the library image instead
+// of a caller-provided workspace.
+namespace hdp {
+namespace {
+
+// Largest SPLIT workspace (partial O and LSE of every causal block) the
+// static area holds; each GPU that loads the library reserves it until exit.
+constexpr size_t kStaticSplitScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_split_scratch[kStaticSplitScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Device address of g_split_scratch on the current device.  Resolved once per
+// device, on the first call made with that device current.
+hdp_status_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(HDP_ERR_UNSUPPORTED, "device index out of range for the static scratch");
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_split_scratch);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(g_split_scratch)");
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return HDP_OK;
+}
+
+}  // namespace
+}  // namespace hdp
+
+extern "C" hdp_status_t hdp_attention_fwd_split_noalloc(hdp_plan_t plan, const void* q, const void* k,
+                                                        const void* v, int32_t hq, int32_t hkv, int32_t d,
+                                                        float scale, void* o, float* lse, void* stream) {
+  if (!plan) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd_split_noalloc: plan is NULL");
+  if (hq < 1 || d < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd_split_noalloc: hq, d must be >= 1");
+  size_t ob = 0, need = 0;
+  split_workspace(plan, hq, d, &ob, &need);
+  if (need > kStaticSplitScratchBytes)
+    return fail(HDP_ERR_INVALID_ARGUMENT,
+                "hdp_attention_fwd_split_noalloc: this plan needs " + std::to_string(need) +
+                    " bytes of SPLIT scratch, more than the static maximum of " +
+                    std::to_string(kStaticSplitScratchBytes) + " bytes; use hdp_attention_fwd with a workspace");
+  void* scratch = nullptr;
+  hdp_status_t r = static_scratch(&scratch);
+  if (r != HDP_OK) return r;
+  return hdp_attention_fwd(plan, q, k, v, hq, hkv, d, scale, HDP_MODE_SPLIT, scratch, kStaticSplitScratchBytes, o,
+                           lse, stream);
+}
