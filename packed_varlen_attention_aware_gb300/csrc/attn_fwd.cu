@@ -43,15 +43,22 @@ hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, co
 
 namespace {
 
-constexpr int kThreads = 320;
+// 12 warps = 3 warpgroups: two softmax warpgroups and one for the producer
+// (warp 8), the MMA issuer (warp 9) and two idle warps.  Launched at 168
+// registers a thread (384 x 168 = 64,512); setmaxnreg then moves registers to
+// the softmax warpgroups: 2 x 128 x 192 + 128 x 120 = 64,512.
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxRegs = 192;
+constexpr int kControlRegs = 120;
 constexpr int kStages = 2;  // K and V ring depth
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 // error codes recorded in the device error word
 constexpr int kErrQFull = 0x101, kErrKFull = 0x102, kErrVFull = 0x103, kErrSFull = 0x104, kErrPFull = 0x105,
-              kErrOFull = 0x106, kErrOEmpty = 0x107, kErrKEmpty = 0x108, kErrVEmpty = 0x109, kErrQEmpty = 0x10a;
+              kErrOFull = 0x106, kErrOEmpty = 0x107, kErrKEmpty = 0x108, kErrVEmpty = 0x109, kErrQEmpty = 0x10a,
+              kErrKvEmpty = 0x10b;
 
 template <int D>
 struct SmemLayout {
@@ -66,8 +73,9 @@ struct SmemLayout {
 
 struct Bars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t kv_full[2];                 // one TMA group: K(j+1) and/or V(j)
+  uint64_t kv_empty[2];                // the MMA thread has consumed that group's phase
+  uint64_t k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;  // private to the MMA thread: completion of all its MMAs at exit
   uint32_t tmem_base;
@@ -150,15 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
       mbar_init(&bars.p_full[s], 4);  // one arrive per softmax warp
-      mbar_init(&bars.o_full[s], 1);
+      mbar_init(&bars.o_full[s], 1);  // completes once per unit (its last P.V)
       mbar_init(&bars.o_empty[s], 4);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
-      mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
     mbar_init(&bars.drain, 1);
@@ -182,13 +190,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [tmem](int slot) { return tmem + static_cast<uint32_t>(slot) * 128u; };
   auto tO = [tmem](int slot) { return tmem + 256u + static_cast<uint32_t>(slot) * D; };
 
+  if (warp >= 8) {
+  // control warpgroup: give registers back first, then split into roles
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
+    // Per unit: Q of both slots, then TMA groups {K(0)}, {V(0), K(1)}, ...,
+    // {V(n-1)}; group j+1 is what the MMA thread needs for its tile-j step
+    // (P.V(j) then S = Q K(j+1)^T), so one wait covers both operands.
     if (lane == 0) {
       uint32_t q_uses[2] = {0, 0};
-      uint32_t kcount[kStages] = {}, vcount[kStages] = {};  // loads issued per stage
-      long long kload = 0, vload = 0;
+      uint32_t gcount[2] = {0, 0};  // groups armed per kv_full barrier
+      long long kload = 0, vload = 0, g = 0;
       bool ok = true;
+      auto arm_group = [&](const Unit& x, int kj, int vj) -> bool {
+        // kj / vj < 0: no K / V tile in this group
+        if (kj >= 0) {
+          const long long round = kload / kStages;
+          if (round > 0 &&
+              !mbar_wait(&bars.k_empty[kload % kStages], (round - 1) & 1, abort_word, p.err, kErrKEmpty))
+            return false;
+        }
+        if (vj >= 0) {
+          const long long round = vload / kStages;
+          if (round > 0 &&
+              !mbar_wait(&bars.v_empty[vload % kStages], (round - 1) & 1, abort_word, p.err, kErrVEmpty))
+            return false;
+        }
+        // A group barrier is re-armed only after the MMA thread has consumed
+        // its previous phase (group g-2).  Free K/V stages do not imply that,
+        // and re-arming earlier could complete two phases before the MMA thread
+        // looks, which it would then miss.
+        uint64_t* bar = &bars.kv_full[g & 1];
+        if (g >= 2 && !mbar_wait(&bars.kv_empty[g & 1], ((g >> 1) - 1) & 1, abort_word, p.err, kErrKvEmpty))
+          return false;
+        mbar_arrive_expect_tx(bar, (kj >= 0 ? L::kTileBytes : 0) + (vj >= 0 ? L::kTileBytes : 0));
+        if (kj >= 0) {
+          uint8_t* dst = smem + L::kK + (kload % kStages) * L::kTileBytes;
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(dst + hb * L::kHalfBytes, &tmK, bar, hb * 64, x.kvh, x.kv_row0 + kj * kTile);
+          ++kload;
+        }
+        if (vj >= 0) {
+          uint8_t* dst = smem + L::kV + (vload % kStages) * L::kTileBytes;
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(dst + hb * L::kHalfBytes, &tmV, bar, hb * 64, x.kvh, x.kv_row0 + vj * kTile);
+          ++vload;
+        }
+        ++gcount[g & 1];
+        ++g;
+        return true;
+      };
       for (long long k = 0; ok; ++k) {
         const long long u = unit_index(k, cta, nctas);
         if (u >= total_units) break;
@@ -204,79 +258,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hb = 0; hb < D / 64; ++hb)
             tma_load_3d(dst + hb * L::kHalfBytes, &tmQ, &bars.q_full[s], hb * 64, x.h0 + s, x.q_row0);
         }
-        for (int j = 0; j < x.ntiles_kv && ok; ++j) {
-          const int row = x.kv_row0 + j * kTile;
-          {
-            const int st = static_cast<int>(kload % kStages);
-            const long long round = kload / kStages;
-            if (round > 0) ok = mbar_wait(&bars.k_empty[st], (round - 1) & 1, abort_word, p.err, kErrKEmpty);
-            if (!ok) break;
-            uint8_t* dst = smem + L::kK + st * L::kTileBytes;
-            mbar_arrive_expect_tx(&bars.k_full[st], L::kTileBytes);
-#pragma unroll
-            for (int hb = 0; hb < D / 64; ++hb)
-              tma_load_3d(dst + hb * L::kHalfBytes, &tmK, &bars.k_full[st], hb * 64, x.kvh, row);
-            ++kload;
-            ++kcount[st];
-          }
-          {
-            const int st = static_cast<int>(vload % kStages);
-            const long long round = vload / kStages;
-            if (round > 0) ok = mbar_wait(&bars.v_empty[st], (round - 1) & 1, abort_word, p.err, kErrVEmpty);
-            if (!ok) break;
-            uint8_t* dst = smem + L::kV + st * L::kTileBytes;
-            mbar_arrive_expect_tx(&bars.v_full[st], L::kTileBytes);
-#pragma unroll
-            for (int hb = 0; hb < D / 64; ++hb)
-              tma_load_3d(dst + hb * L::kHalfBytes, &tmV, &bars.v_full[st], hb * 64, x.kvh, row);
-            ++vload;
-            ++vcount[st];
-          }
-        }
+        if (ok) ok = arm_group(x, 0, -1);
+        for (int j = 0; j < x.ntiles_kv && ok; ++j) ok = arm_group(x, j + 1 < x.ntiles_kv ? j + 1 : -1, j);
       }
       if (!ok) {
-        // drain: every armed full barrier completes once its bytes land
-        for (int st = 0; st < kStages; ++st) {
-          if (kcount[st] > 0) drain_wait(&bars.k_full[st], (kcount[st] - 1) & 1);
-          if (vcount[st] > 0) drain_wait(&bars.v_full[st], (vcount[st] - 1) & 1);
-        }
+        // drain: every armed group barrier completes once its bytes land
+        for (int b = 0; b < 2; ++b)
+          if (gcount[b] > 0) drain_wait(&bars.kv_full[b], (gcount[b] - 1) & 1);
         for (int s = 0; s < 2; ++s)
           if (q_uses[s] > 0) drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
       }
     }
     __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kThreads);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // Issue order per key tile j: P.V of slot 0, then S = Q K^T of slot 0 for
-    // tile j+1, then the same for slot 1.  The softmax of one slot runs while
-    // the tensor core works on the other slot.  S(j+1) of a slot overwrites the
-    // TMEM columns that P(j) of the same slot occupies; the two MMAs are issued
-    // back to back by this thread and execute in issue order.
+    // Per key tile j: wait for its TMA group, then for each slot P.V(j)
+    // followed at once by S = Q K(j+1)^T.  S(j+1) of a slot overwrites the TMEM
+    // columns that P(j) of the same slot occupies; this thread issues the two
+    // back to back and they execute in issue order.  The tensor core's issue
+    // queue is shallow, so this thread keeps waits few and cheap: one per TMA
+    // group, one per P, and commits only where a consumer needs them.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
-      long long kuse = 0, vuse = 0;
-      bool ok = true;
+      // Descriptors: base per buffer; K steps add compile-time offsets to the
+      // start-address field (addresses stay below 256 KB, so no carry).
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
       auto issue_qk = [&](int s, int kst) {
-        const uint32_t qa = sQ + s * L::kTileBytes;
-        const uint32_t kb = sK + kst * L::kTileBytes;
+        const uint64_t qd = dQ + s * kTileUnits, kd = dK + kst * kTileUnits;
+        umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_ss(tS(s), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+          umma_ss_c<true>(tS(s), qd + off, kd + off, idesc_qk);
         }
         umma_commit(&bars.s_full[s]);
       };
       auto issue_pv = [&](int s, int vst, bool accumulate) {
-        const uint32_t vb = sV + vst * L::kTileBytes;
+        const uint64_t vd = dV + vst * kTileUnits;
+        if (accumulate)
+          umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
+        else
+          umma_ts_c<false>(tO(s), tS(s), vd, idesc_pv);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tO(s), tS(s) + kk * 8, sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv,
-                  (accumulate || kk > 0) ? 1u : 0u);
-        umma_commit(&bars.o_full[s]);
+        for (int kk = 1; kk < kTile / 16; ++kk)
+          umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
       };
+      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
+      long long kuse = 0, vuse = 0, g = 0;
+      bool ok = true;
       for (long long k = 0; ok; ++k) {
         const long long u = unit_index(k, cta, nctas);
         if (u >= total_units) break;
@@ -287,11 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&bars.q_full[s], q_uses[s] & 1, abort_word, p.err, kErrQFull);
           ++q_uses[s];
         }
-        // S(0) for both slots
-        int kst = static_cast<int>(kuse % kStages);
-        if (ok) ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
+        // S(0) for both slots.  TMA-written operands need no tcgen05 fence: the
+        // mbarrier completion orders them for the tensor core.
+        if (ok) ok = mbar_wait(&bars.kv_full[g & 1], (g >> 1) & 1, abort_word, p.err, kErrKFull);
+        if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
+        ++g;
         if (!ok) break;
-        tc_fence_after();
+        int kst = static_cast<int>(kuse % kStages);
         for (int s = 0; s < nslots; ++s) {
           issue_qk(s, kst);
           if (n == 1) umma_commit(&bars.q_empty[s]);
@@ -299,8 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars.k_empty[kst]);
         ++kuse;
         for (int j = 0; j < n && ok; ++j) {
+          ok = mbar_wait(&bars.kv_full[g & 1], (g >> 1) & 1, abort_word, p.err, kErrVFull);
+          if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
+          ++g;
           const int vst = static_cast<int>(vuse % kStages);
-          ok = mbar_wait(&bars.v_full[vst], (vuse / kStages) & 1, abort_word, p.err, kErrVFull);
           const bool more = j + 1 < n;
           kst = static_cast<int>(kuse % kStages);
           for (int s = 0; s < nslots && ok; ++s) {
@@ -313,12 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             issue_pv(s, vst, j > 0);
+            if (!more) umma_commit(&bars.o_full[s]);
             if (more) {
-              if (s == 0) {
-                ok = mbar_wait(&bars.k_full[kst], (kuse / kStages) & 1, abort_word, p.err, kErrKFull);
-                if (!ok) break;
-                tc_fence_after();
-              }
               issue_qk(s, kst);
               if (j + 2 == n) umma_commit(&bars.q_empty[s]);
             }
@@ -338,13 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&bars.drain, 0);
     }
     __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kThreads);  // every role is done with TMEM
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else {
+    named_barrier_sync(1, kThreads);  // idle warps of the control warpgroup
+  }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     const int s = warp >> 2;                 // slot
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = tile row
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
-    uint32_t s_count = 0;
+    uint32_t s_count = 0, units_done = 0;
     bool ok = true;
     for (long long k = 0; ok; ++k) {
       const long long u = unit_index(k, cta, nctas);
@@ -393,27 +436,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
           rescale_o = j > 0;
         }
+        // p = 2^(s*scale*log2e - m); 16 independent packed partial sums, the
+        // four 32-column chunks interleaved element by element
         const uint64_t negm2 = pack_f32x2(-m, -m);
-        uint64_t acc[4];
-        uint32_t pk[2][32];
+        uint64_t acc[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          acc[c] = pack_f32x2(0.f, 0.f);
+        for (int q = 0; q < 16; ++q) acc[q] = pack_f32x2(0.f, 0.f);
+        uint32_t pk[4][16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), scale2,
-                                          negm2);
+        for (int i = 0; i < 32; i += 2) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])),
+                                          scale2, negm2);
             const float p0 = ex2_approx(lo_f32(t));
             const float p1 = ex2_approx(hi_f32(t));
-            acc[c] = fadd_f32x2(acc[c], pack_f32x2(p0, p1));
-            pk[c >> 1][(c & 1) * 16 + i / 2] = pack_bf16x2(p0, p1);
+            const int q = c * 4 + ((i >> 1) & 3);
+            acc[q] = fadd_f32x2(acc[q], pack_f32x2(p0, p1));
+            pk[c][i / 2] = pack_bf16x2(p0, p1);
           }
-          if (c == 1) tmem_st32(tS(s) + lane_off, pk[0]);
         }
-        tmem_st32(tS(s) + lane_off + 32, pk[1]);
-        const uint64_t a01 = fadd_f32x2(acc[0], acc[1]), a23 = fadd_f32x2(acc[2], acc[3]);
-        const uint64_t a = fadd_f32x2(a01, a23);
-        l += lo_f32(a) + hi_f32(a);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(tS(s) + lane_off + c * 16, pk[c]);
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int q = 0; q < w; ++q) acc[q] = fadd_f32x2(acc[q], acc[q + w]);
+        l += lo_f32(acc[0]) + hi_f32(acc[0]);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // P.V of tile j-1 is complete: S_s(j) was committed after it
 #pragma unroll 1
@@ -432,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars.p_full[s]);
       }
       if (!ok) break;
-      // ---- epilogue: wait for the last P.V, normalize, store
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[s], (s_count - 1) & 1, abort_word, p.err, kErrOFull));
+      // ---- epilogue: wait for the unit's last P.V, normalize, store
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[s], units_done & 1, abort_word, p.err, kErrOFull));
       if (!ok) break;
       tc_fence_after();
       const bool row_valid = row < x.q_rows;
@@ -481,13 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.o_empty[s]);
+      ++units_done;
     }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tc_fence_before();
+    named_barrier_sync(1, kThreads);
   }
 }
 
