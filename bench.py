@@ -62,12 +62,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def attn_kernel_source_sha256() -> str:
+    """Hash of the attention kernel's device code (the part of attn_fwd.cu
+    before its host-side section, plus the PTX wrapper header)."""
+    src = open(ATTN_SRC).read()
+    cut = src.index("// ---------------------------------------------------------------- host side")
+    ptx = open(os.path.join(os.path.dirname(ATTN_SRC), "sm103_ptx.cuh")).read()
+    return hashlib.sha256((src[:cut] + ptx).encode()).hexdigest()
+
+
 def traffic_from_profile():
     """dram bytes per attention launch from the committed ncu summary, valid
     only while the kernel source is the one that was profiled."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    want = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
+    want = attn_kernel_source_sha256()
     sha, dram = None, None
     for line in open(TRAFFIC_FILE):
         if line.startswith("kernel_source_sha256:"):
@@ -381,6 +390,63 @@ def our_arm(args, ws, rank, local):
     return 0
 
 
+def kernels_mode(args):
+    """Secondary kernels: the plan on 2^24 random lengths and the LSE merge on
+    16 partials of 2^20 rows (d = 128).  CUDA-event times per call; the merge
+    also as HBM GB/s of its algorithmic bytes."""
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    peaks, src = load_peaks()
+    out = {"mode": "kernels", "peak_source": src}
+    g = torch.Generator(device="cuda").manual_seed(args.seed)
+    # plan stress
+    n = 1 << 24
+    lengths = torch.randint(1, 100, (n,), generator=g, device="cuda", dtype=torch.int32)
+    times = []
+    for it in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        plan = pkg.hdp_plan_create(lengths, 64, flags=pkg.HDP_PLAN_NO_SHARDS)
+        e1.record()
+        torch.cuda.synchronize()
+        if it:
+            times.append(e0.elapsed_time(e1))
+        v = plan.view
+        plan.destroy()
+    scan_bytes = 4 * n * 2 + (n + 1) * (4 + 4 + 8 + 8 + 8) + 8 * v.num_tiles_fused * 4
+    out["plan_stress"] = {"docs": n, "capacity": 64, "ms_per_call": statistics.median(times),
+                          "num_chunks": v.num_chunks, "num_blocks": v.num_blocks,
+                          "note": "whole hdp_plan_create incl. host sync, allocation and the work-list sort; "
+                                  "per-kernel HBM rates come from the ncu launch list"}
+    # merge
+    m, rows, d = 16, 1 << 20, 128
+    o_parts = torch.randn(m, rows, d, generator=g, device="cuda", dtype=torch.float32)
+    lse_parts = torch.randn(m, rows, generator=g, device="cuda", dtype=torch.float32) * 2
+    o = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    times = []
+    for it in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkg.hdp_lse_merge_rows(o_parts, lse_parts, o, lse)
+        e1.record()
+        torch.cuda.synchronize()
+        if it:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    nbytes = m * rows * (4 * d + 4) + rows * (2 * d + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["lse_merge"] = {"m": m, "rows": rows, "d": d, "ms_per_call": ms, "algorithmic_bytes": nbytes,
+                        "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,10 +458,13 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true", help="time the plan stress input and the LSE merge")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
+    if args.kernels:
+        return kernels_mode(args) if rank == 0 else 0
     if args.impl == "reference":
         return reference_arm(args, rank)
     return our_arm(args, ws, rank, local)

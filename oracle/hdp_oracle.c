@@ -152,7 +152,12 @@ int oracle_plan(const int32_t* lengths, int32_t n, int32_t C, int32_t* cu_seqlen
   chunk_offsets[n] = (int32_t)ch;
   block_offsets[n] = blk;
 
-  /* shards: full chunks first, in chunk order */
+  /* shards: full chunks first, in chunk order (skipped when the caller passes
+   * shard_of_chunk = NULL) */
+  if (!shard_of_chunk) {
+    *num_shards = 0;
+    return ORC_OK;
+  }
   int32_t ns = 0;
   int64_t npieces = 0;
   for (int64_t c = 0; c < ch; c++) {

@@ -85,8 +85,9 @@ def plan_sizes(lengths, C: int):
     return int(nc[0]), int(nb[0]), int(tt[0])
 
 
-def plan(lengths, C: int) -> dict:
-    """Sharding plan of section 3.1 (see hdp_oracle.c for the tables)."""
+def plan(lengths, C: int, shards: bool = True) -> dict:
+    """Sharding plan of section 3.1 (see hdp_oracle.c for the tables).
+    shards=False skips best-fit packing (quadratic in the number of pieces)."""
     lib = _load()
     L = np.ascontiguousarray(lengths, dtype=np.int32)
     n = len(L)
@@ -103,7 +104,7 @@ def plan(lengths, C: int) -> dict:
     ns = np.zeros(1, np.int32)
     rc = lib.oracle_plan(_ptr(L), n, int(C), _ptr(out["cu_seqlens"]), _ptr(out["chunk_offsets"]),
                          _ptr(out["block_offsets"]), _ptr(out["chunk_table"]), _ptr(out["block_table"]),
-                         _ptr(out["chunk_pairs"]), _ptr(out["shard_of_chunk"]), _ptr(ns))
+                         _ptr(out["chunk_pairs"]), _ptr(out["shard_of_chunk"]) if shards else None, _ptr(ns))
     if rc != 0:
         raise ValueError(f"oracle_plan failed (rc={rc})")
     out["chunk_table"] = out["chunk_table"][:nc]

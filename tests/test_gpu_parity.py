@@ -155,3 +155,52 @@ def test_seq128k_sampled(mode):
     o, lse, plan = run_gpu(q, k, v, list(w.lengths), w.capacity, mode)
     toks, heads = sample_rows(list(w.lengths), w.hq, 200, 7)
     sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq128k mode {mode}")
+
+
+def test_mix1m_sampled():
+    """1M-token skewed mixture, C = 8192, FUSED, sampled rows of every length class."""
+    w = wl.workload("mix1m")
+    q, k, v = wl.qkv(w, device="cuda")
+    o, lse, plan = run_gpu(q, k, v, list(w.lengths), w.capacity, FUSED)
+    rng = np.random.default_rng(3)
+    cu = np.concatenate([[0], np.cumsum(w.lengths)])
+    toks = []
+    order = np.argsort(w.lengths)
+    for i in list(order[:5]) + list(order[-5:]):  # shortest and longest documents
+        s = w.lengths[i]
+        toks += [cu[i], cu[i] + s - 1, cu[i] + rng.integers(0, s)]
+    toks = np.array(toks + list(rng.integers(0, w.total_tokens, 120)), dtype=np.int64)
+    heads = rng.integers(0, w.hq, len(toks)).astype(np.int32)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, "mix1m")
+
+
+def test_seq2m_sampled_chunks():
+    """2M-token sequence, C = 8192, FUSED over all 256 chunks; the oracle checks
+    rows of four query chunks: the first, the last and two drawn at random."""
+    w = wl.workload("seq2m")
+    q, k, v = wl.qkv(w, device="cuda")
+    o, lse, plan = run_gpu(q, k, v, list(w.lengths), w.capacity, FUSED)
+    rng = np.random.default_rng(w.seed)
+    C = w.capacity
+    chunks = [0, 255] + list(rng.choice(np.arange(1, 255), 2, replace=False))
+    toks = []
+    for c in chunks:
+        toks += [c * C, c * C + C - 1, c * C + 127, c * C + 128] + list(c * C + rng.integers(0, C, 6))
+    toks = np.array(toks, dtype=np.int64)
+    heads = rng.integers(0, w.hq, len(toks)).astype(np.int32)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq2m chunks {chunks}")
+
+
+def test_plan_stress_many_documents():
+    """2^24 random lengths (plan scan over 8,192 CTAs of documents), without shards."""
+    rng = np.random.default_rng(24)
+    lengths = rng.integers(1, 100, 1 << 24).astype(np.int32)
+    dl = torch.from_numpy(lengths).cuda()
+    with pkg.hdp_plan_create(dl, 64, flags=pkg.HDP_PLAN_NO_SHARDS) as plan:
+        ref = oracle.plan(lengths, 64, shards=False)
+        v = plan.view
+        assert (v.num_chunks, v.num_blocks, v.total_tokens) == (ref["num_chunks"], ref["num_blocks"],
+                                                                 int(ref["cu_seqlens"][-1]))
+        got = plan.tables()
+        for key in ("cu_seqlens", "chunk_offsets", "block_offsets", "chunk_table", "block_table", "chunk_pairs"):
+            assert np.array_equal(got[key], ref[key]), key
