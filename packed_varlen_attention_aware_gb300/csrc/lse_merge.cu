@@ -52,21 +52,32 @@ __device__ __forceinline__ float merge_row(int m, int d, int lane, LseAt lse_at,
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     L = M + logf(sum);
-    for (int k = 0; k < m; ++k) {
-      const float w = expf(lse_at(k) - L);
-      if (w == 0.f) continue;
-      const float* ok = o_at(k);
+    // four partials per step: their loads are independent, so up to four
+    // 512-byte rows per warp are in flight
+    for (int k0 = 0; k0 < m; k0 += 4) {
+      float w[4];
+      float4 x[4][VEC];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        const int c = (v * 32 + lane) * 4;
-        if (c < d) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(ok + c));
-          acc[v].x = fmaf(w, x.x, acc[v].x);
-          acc[v].y = fmaf(w, x.y, acc[v].y);
-          acc[v].z = fmaf(w, x.z, acc[v].z);
-          acc[v].w = fmaf(w, x.w, acc[v].w);
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u;
+        w[u] = k < m ? expf(lse_at(k) - L) : 0.f;
+        const float* ok = o_at(k < m ? k : k0);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+          const int c = (v * 32 + lane) * 4;
+          x[u][v] = (c < d && w[u] != 0.f) ? __ldg(reinterpret_cast<const float4*>(ok + c))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+          acc[v].x = fmaf(w[u], x[u][v].x, acc[v].x);
+          acc[v].y = fmaf(w[u], x[u][v].y, acc[v].y);
+          acc[v].z = fmaf(w[u], x[u][v].z, acc[v].z);
+          acc[v].w = fmaf(w[u], x[u][v].w, acc[v].w);
+        }
     }
   }
 #pragma unroll

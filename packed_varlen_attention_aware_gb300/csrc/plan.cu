@@ -37,21 +37,24 @@ constexpr int kIdxBits = 40;
 constexpr unsigned long long kIdxMask = (1ull << kIdxBits) - 1;
 constexpr long long kWeightCap = 1ll << 24;  // > max tiles of a document (2^31 / 128)
 
+// Per-document quantities (s >= 1).  32-bit unsigned division: every
+// intermediate is below 2^31 for s, C < 2^31.
 __device__ __forceinline__ void doc_quantities(int32_t s, int32_t C, bool split_ok, long long (&q)[kQ]) {
-  const long long n = (static_cast<long long>(s) + C - 1) / C;
+  const uint32_t su = static_cast<uint32_t>(s), cu = static_cast<uint32_t>(C);
+  const uint32_t n = (su - 1u) / cu + 1u;   // ceil(s / C)
+  const uint32_t last = su - (n - 1u) * cu;  // length of the last chunk, in [1, C]
   q[0] = s;
   q[1] = n;
-  q[2] = n * (n + 1) / 2;
-  q[3] = (static_cast<long long>(s) + kTile - 1) / kTile;
+  q[2] = static_cast<long long>(n) * (n + 1) / 2;
+  q[3] = (su + kTile - 1) / kTile;
   if (split_ok) {
-    const long long tpc = C / kTile;
-    const long long last = s - (n - 1) * static_cast<long long>(C);
+    const long long tpc = cu / kTile;
     const long long tl = (last + kTile - 1) / kTile;
-    q[4] = tpc * ((n - 1) * n / 2) + tl * n;
+    q[4] = tpc * (static_cast<long long>(n - 1) * n / 2) + tl * n;
   } else {
     q[4] = 0;
   }
-  q[5] = (s % C) != 0 ? 1 : 0;
+  q[5] = last != cu ? 1 : 0;
 }
 
 // Exclusive scan of N int64 values over a 256-thread block; also returns the
@@ -220,22 +223,56 @@ __global__ void __launch_bounds__(kScanThreads) k_plan_scan_write(const int32_t*
   const long long* p = partials + static_cast<long long>(blockIdx.x) * kPartial;
 #pragma unroll
   for (int k = 0; k < kQ; ++k) sum[k] += p[k];
+  // this thread's 8 consecutive documents: exclusive prefixes in registers,
+  // then 16-byte stores
+  const long long first = base + threadIdx.x * kScanItems;
+  int32_t vcu[kScanItems], vco[kScanItems], vpo[kScanItems];
+  long long vbo[kScanItems], vtf[kScanItems], vts[kScanItems];
 #pragma unroll
   for (int j = 0; j < kScanItems; ++j) {
-    const long long i = base + threadIdx.x * kScanItems + j;
-    if (i < n) {
-      cu[i] = static_cast<int32_t>(sum[0]);
-      co[i] = static_cast<int32_t>(sum[1]);
-      bo[i] = sum[2];
-      tof[i] = sum[3];
-      tos[i] = sum[4];
-      po[i] = static_cast<int32_t>(sum[5]);
-      const int32_t s = s_len[threadIdx.x * kScanItems + j];
-      if (s >= 1) {
-        long long q[kQ];
-        doc_quantities(s, C, split_ok != 0, q);
+    vcu[j] = static_cast<int32_t>(sum[0]);
+    vco[j] = static_cast<int32_t>(sum[1]);
+    vbo[j] = sum[2];
+    vtf[j] = sum[3];
+    vts[j] = sum[4];
+    vpo[j] = static_cast<int32_t>(sum[5]);
+    const int32_t s = s_len[threadIdx.x * kScanItems + j];
+    if (first + j < n && s >= 1) {
+      long long q[kQ];
+      doc_quantities(s, C, split_ok != 0, q);
 #pragma unroll
-        for (int k = 0; k < kQ; ++k) sum[k] += q[k];
+      for (int k = 0; k < kQ; ++k) sum[k] += q[k];
+    }
+  }
+  if (first + kScanItems <= n) {
+    int4* c4 = reinterpret_cast<int4*>(cu + first);
+    int4* o4 = reinterpret_cast<int4*>(co + first);
+    int4* p4 = reinterpret_cast<int4*>(po + first);
+    c4[0] = make_int4(vcu[0], vcu[1], vcu[2], vcu[3]);
+    c4[1] = make_int4(vcu[4], vcu[5], vcu[6], vcu[7]);
+    o4[0] = make_int4(vco[0], vco[1], vco[2], vco[3]);
+    o4[1] = make_int4(vco[4], vco[5], vco[6], vco[7]);
+    p4[0] = make_int4(vpo[0], vpo[1], vpo[2], vpo[3]);
+    p4[1] = make_int4(vpo[4], vpo[5], vpo[6], vpo[7]);
+    longlong2* b2 = reinterpret_cast<longlong2*>(bo + first);
+    longlong2* f2 = reinterpret_cast<longlong2*>(tof + first);
+    longlong2* s2 = reinterpret_cast<longlong2*>(tos + first);
+#pragma unroll
+    for (int j = 0; j < kScanItems / 2; ++j) {
+      b2[j] = make_longlong2(vbo[2 * j], vbo[2 * j + 1]);
+      f2[j] = make_longlong2(vtf[2 * j], vtf[2 * j + 1]);
+      s2[j] = make_longlong2(vts[2 * j], vts[2 * j + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+      if (first + j < n) {
+        cu[first + j] = vcu[j];
+        co[first + j] = vco[j];
+        po[first + j] = vpo[j];
+        bo[first + j] = vbo[j];
+        tof[first + j] = vtf[j];
+        tos[first + j] = vts[j];
       }
     }
   }
