@@ -4,9 +4,10 @@
 // only to its own sequence; each C x C block of a long sequence is a partial
 // result, and partials are combined by log-sum-exp).
 //
-// Design (one persistent CTA per SM, 10 warps):
+// Design (one persistent CTA per SM, 12 warps):
 //   warps 0-3  softmax for query slot 0     warps 4-7  softmax for query slot 1
 //   warp 8     TMA producer                 warp 9     MMA issuer + TMEM owner
+//   warp 10    waits on behalf of the MMA issuer
 // A work unit is one query tile (128 rows of one document, from the plan's
 // heaviest-first work list) for one key/value head and a pair of query heads of
 // that head's GQA group: both slots share every K/V tile.  Only the key tiles
@@ -44,12 +45,14 @@ hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, co
 namespace {
 
 // 12 warps = 3 warpgroups: two softmax warpgroups and one for the producer
-// (warp 8), the MMA issuer (warp 9) and two idle warps.  Launched at 168
-// registers a thread (384 x 168 = 64,512); setmaxnreg then moves registers to
+// (warp 8), the MMA issuer (warp 9), its waiter (warp 10) and an idle warp.
+// Launched at 168 registers a thread (384 x 168 = 64,512); setmaxnreg then moves registers to
 // the softmax warpgroups: 2 x 128 x 192 + 128 x 120 = 64,512.
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kWaitWarp = 10;
+constexpr uint32_t kHandoffBarrier = 2;  // named barrier between the waiter and MMA warps
 constexpr int kSoftmaxRegs = 192;
 constexpr int kControlRegs = 120;
 constexpr int kStages = 2;  // K and V ring depth
@@ -272,85 +275,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     named_barrier_sync(1, kThreads);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per key tile j: wait for its TMA group, then for each slot P.V(j)
-    // followed at once by S = Q K(j+1)^T.  S(j+1) of a slot overwrites the TMEM
-    // columns that P(j) of the same slot occupies; this thread issues the two
-    // back to back and they execute in issue order.  The tensor core's issue
-    // queue is shallow, so this thread keeps waits few and cheap: one per TMA
-    // group, one per P, and commits only where a consumer needs them.
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      // Descriptors: base per buffer; K steps add compile-time offsets to the
-      // start-address field (addresses stay below 256 KB, so no carry).
-      const uint64_t dQ = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-      const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-      auto issue_qk = [&](int s, int kst) {
-        const uint64_t qd = dQ + s * kTileUnits, kd = dK + kst * kTileUnits;
-        umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
+  } else if (warp == kMmaWarp || warp == kWaitWarp) {
+    // ------------------------------------------------------------ MMA issuer + waiter
+    // Per key tile j: for each slot P.V(j) followed at once by S = Q K(j+1)^T.
+    // S(j+1) of a slot overwrites the TMEM columns that P(j) of the same slot
+    // occupies; one thread issues the two back to back and they execute in
+    // issue order.
+    //
+    // The tensor core's issue queue is shallow, and an mbarrier poll by the
+    // issuing thread lets it run dry.  So the waiter warp performs every
+    // mbarrier wait the MMA stream depends on, in the order the stream consumes
+    // them, and hands each finished wait to the MMA warp through a named
+    // barrier, which carries no such cost.  Both warps walk the same units and
+    // tiles and pass the same handoffs; the barrier also ORs a failure flag, so
+    // a timed-out wait stops both warps at the same handoff.
+    const bool issuer = warp == kMmaWarp && lane == 0;
+    const bool waiter = warp == kWaitWarp && lane == 0;
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+    // Descriptors: base per buffer; K steps add compile-time offsets to the
+    // start-address field (addresses stay below 256 KB, so no carry).
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
+    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+    auto issue_qk = [&](int s, int kst) {
+      const uint64_t qd = dQ + s * kTileUnits, kd = dK + kst * kTileUnits;
+      umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
 #pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
-          umma_ss_c<true>(tS(s), qd + off, kd + off, idesc_qk);
-        }
-        umma_commit(&bars.s_full[s]);
-      };
-      auto issue_pv = [&](int s, int vst, bool accumulate) {
-        const uint64_t vd = dV + vst * kTileUnits;
-        if (accumulate)
-          umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
-        else
-          umma_ts_c<false>(tO(s), tS(s), vd, idesc_pv);
+      for (int kk = 1; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+        umma_ss_c<true>(tS(s), qd + off, kd + off, idesc_qk);
+      }
+      umma_commit(&bars.s_full[s]);
+    };
+    auto issue_pv = [&](int s, int vst, bool accumulate) {
+      const uint64_t vd = dV + vst * kTileUnits;
+      if (accumulate)
+        umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
+      else
+        umma_ts_c<false>(tO(s), tS(s), vd, idesc_pv);
 #pragma unroll
-        for (int kk = 1; kk < kTile / 16; ++kk)
-          umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
-      };
-      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
-      long long kuse = 0, vuse = 0, g = 0;
-      bool ok = true;
-      for (long long k = 0; ok; ++k) {
-        const long long u = unit_index(k, cta, nctas);
-        if (u >= total_units) break;
-        const Unit x = load_unit(p, u);
-        const int nslots = x.valid1 ? 2 : 1;
-        const int n = x.ntiles_kv;
-        for (int s = 0; s < nslots && ok; ++s) {
-          ok = mbar_wait(&bars.q_full[s], q_uses[s] & 1, abort_word, p.err, kErrQFull);
-          ++q_uses[s];
-        }
-        // S(0) for both slots.  TMA-written operands need no tcgen05 fence: the
-        // mbarrier completion orders them for the tensor core.
-        if (ok) ok = mbar_wait(&bars.kv_full[g & 1], (g >> 1) & 1, abort_word, p.err, kErrKFull);
-        if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
-        ++g;
-        if (!ok) break;
-        int kst = static_cast<int>(kuse % kStages);
+      for (int kk = 1; kk < kTile / 16; ++kk)
+        umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
+    };
+    uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
+    long long kuse = 0, vuse = 0, g = 0;
+    bool ok = true;  // the waiter's own waits so far
+    auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
+      if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code);
+    };
+    auto wait_group = [&](int code) {  // one TMA group; the producer may re-arm its barrier afterwards
+      wait_on(&bars.kv_full[g & 1], (g >> 1) & 1, code);
+      if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
+    };
+    // Both warps, all lanes.  True when every wait so far succeeded; the MMA
+    // warp then orders its next tcgen05 operations after the waits.
+    auto handoff = [&]() -> bool {
+      __syncwarp();
+      const bool failed = named_barrier_or(kHandoffBarrier, 64, !ok);
+      tc_fence_after();
+      return !failed;
+    };
+    bool alive = true;
+    for (long long k = 0; alive; ++k) {
+      const long long u = unit_index(k, cta, nctas);
+      if (u >= total_units) break;
+      const Unit x = load_unit(p, u);
+      const int nslots = x.valid1 ? 2 : 1;
+      const int n = x.ntiles_kv;
+      // handoff: Q of every slot and the group holding K(0)
+      if (waiter) {
+        for (int s = 0; s < nslots; ++s) wait_on(&bars.q_full[s], q_uses[s] & 1, kErrQFull);
+        wait_group(kErrKFull);
+      }
+      for (int s = 0; s < nslots; ++s) ++q_uses[s];
+      ++g;
+      if (!handoff()) break;
+      int kst = static_cast<int>(kuse % kStages);
+      if (issuer) {
         for (int s = 0; s < nslots; ++s) {
           issue_qk(s, kst);
           if (n == 1) umma_commit(&bars.q_empty[s]);
         }
         umma_commit(&bars.k_empty[kst]);
-        ++kuse;
-        for (int j = 0; j < n && ok; ++j) {
-          ok = mbar_wait(&bars.kv_full[g & 1], (g >> 1) & 1, abort_word, p.err, kErrVFull);
-          if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
-          ++g;
-          const int vst = static_cast<int>(vuse % kStages);
-          const bool more = j + 1 < n;
-          kst = static_cast<int>(kuse % kStages);
-          for (int s = 0; s < nslots && ok; ++s) {
-            // P_s(j) written (and O_s rescaled) by the softmax warps
-            ok = mbar_wait(&bars.p_full[s], p_uses[s] & 1, abort_word, p.err, kErrPFull);
-            ++p_uses[s];
-            // the first P.V of a unit overwrites O_s: the previous epilogue must have read it
-            if (ok && j == 0 && units_done[s] > 0)
-              ok = mbar_wait(&bars.o_empty[s], (units_done[s] - 1) & 1, abort_word, p.err, kErrOEmpty);
-            if (!ok) break;
-            tc_fence_after();
+      }
+      ++kuse;
+      for (int j = 0; j < n && alive; ++j) {
+        const int vst = static_cast<int>(vuse % kStages);
+        const bool more = j + 1 < n;
+        kst = static_cast<int>(kuse % kStages);
+        for (int s = 0; s < nslots; ++s) {
+          // handoff: (slot 0) the group holding V(j) and K(j+1); P_s(j)
+          // written and O_s rescaled by the softmax warps; and, before the
+          // first P.V of a unit overwrites O_s, the previous epilogue's read
+          if (waiter) {
+            if (s == 0) wait_group(kErrVFull);
+            wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);
+            if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
+          }
+          if (s == 0) ++g;
+          ++p_uses[s];
+          if (!handoff()) {
+            alive = false;
+            break;
+          }
+          if (issuer) {
             issue_pv(s, vst, j > 0);
             if (!more) umma_commit(&bars.o_full[s]);
             if (more) {
@@ -358,16 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j + 2 == n) umma_commit(&bars.q_empty[s]);
             }
           }
-          if (!ok) break;
-          if (more) {
-            umma_commit(&bars.k_empty[kst]);
-            ++kuse;
-          }
-          umma_commit(&bars.v_empty[vst]);
-          ++vuse;
         }
-        for (int s = 0; s < nslots; ++s) ++units_done[s];
+        if (!alive) break;
+        if (more) {
+          if (issuer) umma_commit(&bars.k_empty[kst]);
+          ++kuse;
+        }
+        if (issuer) umma_commit(&bars.v_empty[vst]);
+        ++vuse;
       }
+      if (alive)
+        for (int s = 0; s < nslots; ++s) ++units_done[s];
+    }
+    if (issuer) {
       // drain every MMA this thread issued before TMEM is released
       umma_commit(&bars.drain);
       drain_wait(&bars.drain, 0);
@@ -375,10 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     named_barrier_sync(1, kThreads);  // every role is done with TMEM
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if (warp == kMmaWarp) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
   } else {
-    named_barrier_sync(1, kThreads);  // idle warps of the control warpgroup
+    named_barrier_sync(1, kThreads);  // idle warp of the control warpgroup
   }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
