@@ -439,26 +439,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_count;
         tc_fence_after();
+        // S rows with their per-chunk maxima from the load itself.  A long
+        // arithmetic chain here would also take issue slots from the MMA warp,
+        // which shares a scheduler with one softmax warp of each slot.
         uint32_t r[4][32];
+        float mc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS(s) + lane_off + c * 32, r[c]);
+        for (int c = 0; c < 4; ++c) mc[c] = tmem_ld32_max(tS(s) + lane_off + c * 32, r[c]);
         tmem_wait_ld();
         const int lim = key_limit - j * kTile;
         if (lim < kTile) {
+          // tile crossing the diagonal or the end of the key range: mask, and
+          // take the maximum over the allowed keys only
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
-        }
-        // row max: four independent chains of 3-input max
-        float mc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          mc[c] = __uint_as_float(r[c][0]);
+          for (int c = 0; c < 4; ++c) {
+            mc[c] = __uint_as_float(r[c][0]);
 #pragma unroll
-          for (int i = 1; i < 31; i += 2) mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-          mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+            for (int i = 1; i < 31; i += 2)
+              mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+            mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+          }
         }
         const float mt = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
         const float mt_scaled = mt * p.scale_log2;
