@@ -219,6 +219,67 @@ const char* hdp_last_error_message(void);
  * devices, all threads).  Diagnostic counter; never reset. */
 uint64_t hdp_kernel_launch_count(void);
 
+/* ====================================================================== */
+/* Cost models (host arithmetic only: no device, no stream, no allocation).
+ * "ByteScale: ..." research digest, section 3.2 (ring timing model and its
+ * table of worked cases) and section 3.3 (cost models T(s), Act(s) and
+ * Eq. 3).  Times and bandwidths are in any consistent units. */
+
+/*
+ * Per-step compute of a ring of N ranks holding C tokens each (section 3.2):
+ *   t_c = t_blk * sum_i (s_i / (N C))^2
+ * where every sequence of the pack is cut into N slices and a query attends
+ * only to its own sequence; t_blk is the time of one full C x C block.
+ * lengths: host int32[n], n >= 1, every s_i >= 1, sum s_i <= N * C.
+ * INVALID_ARGUMENT otherwise (or t_blk < 0, or a null pointer).
+ */
+hdp_status_t hdp_ring_step_compute(const int32_t* lengths, int32_t n, int32_t num_ranks, int32_t capacity,
+                                   double t_blk, double* t_c);
+
+/*
+ * Attention time of that ring (section 3.2): each step overlaps the transfer
+ * of the next K/V slice (t_x) with the compute on the current one (t_c):
+ *   T_attn = (N - 1) * max(t_c, t_x) + t_c.
+ * num_ranks >= 1, t_c >= 0, t_x >= 0.
+ */
+hdp_status_t hdp_ring_attention_time(int32_t num_ranks, double t_c, double t_x, double* t_attn);
+
+/* Profiled cost models of section 3.3, T(s) = alpha1 s^2 + beta1 s + gamma
+ * (time of one layer on a sequence of s tokens) and
+ * Act(s) = alpha2 s + beta2 (activation bytes of one layer), with the
+ * device-to-host and host-to-device copy bandwidths (bytes per time unit)
+ * and l layers per rank. */
+typedef struct {
+  double alpha1, beta1, gamma;
+  double alpha2, beta2;
+  double bw_d2h, bw_h2d;
+  int32_t layers; /* l >= 3 */
+} hdp_offload_model_t;
+
+/*
+ * Selective offloading, Eq. 3 (section 3.3): the rank count of a sequence of
+ * s tokens when a fraction r of the activations of l - 2 of its l layers is
+ * kept in host memory,
+ *   D(s) = ceil((2 Act(s) + (1 - r)(l - 2) Act(s)) / (l Act(C))),
+ * subject to the copy hiding behind compute, T(s) >= r Act(s) / min(B_d2h, B_h2d),
+ * and to 1 >= r >= min(1, l Act(C) / ((l - 2) Act(s))).  D does not grow with r,
+ * so the rank count is smallest at the largest admissible ratio:
+ *   r = min(1, T(s) min(B_d2h, B_h2d) / Act(s)) when that is at least the lower
+ *   bound, else r = 0 (no offloading, D = ceil(Act(s) / Act(C))).
+ * Requires s >= 1, capacity >= 1, layers >= 3, Act(C) > 0, Act(s) > 0,
+ * bandwidths >= 0.  Outputs the chosen ratio and rank count.
+ */
+hdp_status_t hdp_offload_ranks(const hdp_offload_model_t* model, int64_t s, int64_t capacity, double* r,
+                               int64_t* ranks);
+
+/*
+ * Least-squares fit of a profiled cost model (section 3.3): the polynomial of
+ * the given degree (1: Act(s) = c1 s + c0; 2: T(s) = c2 s^2 + c1 s + c0)
+ * through n points (x_i, y_i); coef[k] is the coefficient of x^k.  n > degree
+ * and at least degree + 1 distinct x values; coef has degree + 1 entries.
+ */
+hdp_status_t hdp_fit_cost_model(const double* x, const double* y, int32_t n, int32_t degree, double* coef);
+
 #ifdef __cplusplus
 }
 #endif
