@@ -482,6 +482,78 @@ def kernels_mode(args):
     return 0
 
 
+def cost_model_mode(args):
+    """Calibrates the cost models of the research digest (sections 3.2-3.3) on
+    this GPU: times the attention of one document of s tokens (Hq = 32,
+    Hkv = 8, d = 128, FUSED) for several s, fits T(s) = alpha1 s^2 + beta1 s +
+    gamma with the library's hdp_fit_cost_model, and derives the time of one
+    full C x C block, t_blk = 2 alpha1 C^2 (a causal document of s tokens has
+    about s^2/2 query-key pairs, a full block C^2).  It then applies the ring
+    model (hdp_ring_step_compute / hdp_ring_attention_time) with this t_blk
+    and the pages' measured transfer t_x = 1.5 ms: the static 256-rank ring's
+    shortest hidden length, and whether an HDP ring of one long sequence hides
+    its transfers.  One JSON line."""
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    hq, hkv, d, C = 32, 8, 128, 8192
+    lengths = [4096, 8192, 16384, 32768, 65536, 131072]
+    g = torch.Generator(device="cuda").manual_seed(args.seed)
+    points = []
+    for s in lengths:
+        q = torch.randn(s, hq, d, generator=g, device="cuda").to(torch.bfloat16)
+        k = torch.randn(s, hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+        v = torch.randn(s, hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+        dl = torch.tensor([s], dtype=torch.int32, device="cuda")
+        plan = pkg.hdp_plan_create(dl, C)
+        o = torch.empty_like(q)
+        lse = torch.empty(hq, s, dtype=torch.float32, device="cuda")
+        times = []
+        for it in range(3 + 5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pkg.hdp_attention_fwd(plan, q, k, v, hq, hkv, d, 1.0 / math.sqrt(d), pkg.HDP_MODE_FUSED, None, o, lse)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= 3:
+                times.append(e0.elapsed_time(e1))
+        pkg.hdp_device_status()
+        plan.destroy()
+        ms = statistics.median(times)
+        flops = 4 * d * hq * s * (s + 1) // 2
+        points.append({"s": s, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12})
+        del q, k, v, o, lse
+    x = [p["s"] for p in points]
+    y = [p["ms"] for p in points]
+    coef = pkg.hdp_fit_cost_model(x, y, 2)
+    alpha1, beta1, gamma = float(coef[2]), float(coef[1]), float(coef[0])
+    t_blk = 2.0 * alpha1 * C * C
+    t_x = 1.5
+    N, s_max = 256, 256 * C
+    # static ring: packs of equal lengths that divide S_max
+    hidden = [s for s in (1 << e for e in range(10, 22))
+              if pkg.hdp_ring_step_compute([s] * (s_max // s), N, C, t_blk) >= t_x]
+    hdp_t_c = pkg.hdp_ring_step_compute([39 * C], 39, C, t_blk)
+    out = {"mode": "cost_model", "unit": "ms", "workload": f"one document of s tokens, Hq={hq}, Hkv={hkv}, "
+           f"d={d}, FUSED, bf16", "points": points,
+           "fit": {"alpha1": alpha1, "beta1": beta1, "gamma": gamma,
+                   "max_rel_residual": max(abs(alpha1 * p["s"] ** 2 + beta1 * p["s"] + gamma - p["ms"]) / p["ms"]
+                                           for p in points)},
+           "t_blk_ms": t_blk, "capacity": C,
+           "ring_model_at_t_x_1.5ms": {
+               "static_256_ring_shortest_hidden_pow2_length": min(hidden) if hidden else None,
+               "static_256_ring_shortest_hidden_length_closed_form": t_x / t_blk * s_max,
+               "hdp_39_rank_ring_t_c_ms": hdp_t_c,
+               "hdp_39_rank_ring_T_attn_ms": pkg.hdp_ring_attention_time(39, hdp_t_c, t_x),
+               "hdp_ring_hides": t_blk >= t_x}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -494,12 +566,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="time the plan stress input and the LSE merge")
+    ap.add_argument("--cost-model", action="store_true",
+                    help="calibrate T(s) and t_blk on this GPU and apply the ring model")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
     if args.kernels:
         return kernels_mode(args) if rank == 0 else 0
+    if args.cost_model:
+        return cost_model_mode(args) if rank == 0 else 0
     if args.impl == "reference":
         return reference_arm(args, rank)
     return our_arm(args, ws, rank, local)

@@ -24,20 +24,25 @@ from .binding import (  # noqa: F401
     HDP_PLAN_DEFAULT,
     HDP_PLAN_NO_SHARDS,
     HdpError,
+    OffloadModel,
     Plan,
     hdp_attention_fwd,
     hdp_attention_fwd_split_noalloc,
     hdp_attention_workspace_bytes,
     hdp_device_status,
+    hdp_fit_cost_model,
     hdp_flops_per_shard,
     hdp_kernel_launch_count,
     hdp_last_error_message,
     hdp_lse_merge,
     hdp_lse_merge_rows,
+    hdp_offload_ranks,
     hdp_plan_create,
     hdp_plan_create_ex,
     hdp_plan_destroy,
     hdp_plan_view,
+    hdp_ring_attention_time,
+    hdp_ring_step_compute,
     hdp_status_string,
     load,
 )

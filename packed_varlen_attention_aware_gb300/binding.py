@@ -30,7 +30,15 @@ EXPORTED = (
     "hdp_attention_workspace_bytes", "hdp_attention_fwd", "hdp_lse_merge", "hdp_lse_merge_rows",
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
     "hdp_kernel_launch_count", "hdp_attention_fwd_split_noalloc",
+    "hdp_ring_step_compute", "hdp_ring_attention_time", "hdp_offload_ranks", "hdp_fit_cost_model",
 )
+
+
+class OffloadModel(ctypes.Structure):
+    """hdp_offload_model_t: T(s) = alpha1 s^2 + beta1 s + gamma, Act(s) = alpha2 s + beta2."""
+    _fields_ = [("alpha1", ctypes.c_double), ("beta1", ctypes.c_double), ("gamma", ctypes.c_double),
+                ("alpha2", ctypes.c_double), ("beta2", ctypes.c_double), ("bw_d2h", ctypes.c_double),
+                ("bw_h2d", ctypes.c_double), ("layers", ctypes.c_int32)]
 
 
 class HdpError(RuntimeError):
@@ -81,6 +89,11 @@ def load(path: str | None = None):
             "hdp_device_status": [V],
             "hdp_status_string": [ctypes.c_int],
             "hdp_last_error_message": [],
+            "hdp_ring_step_compute": [V, I32, I32, I32, ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
+            "hdp_ring_attention_time": [I32, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
+            "hdp_offload_ranks": [ctypes.POINTER(OffloadModel), I64, I64, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(I64)],
+            "hdp_fit_cost_model": [V, V, I32, I32, V],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -257,3 +270,49 @@ def hdp_kernel_launch_count() -> int:
 
 def hdp_last_error_message() -> str:
     return load().hdp_last_error_message().decode(errors="replace")
+
+
+# ---------------------------------------------------------------- cost models (host arithmetic)
+
+def hdp_ring_step_compute(lengths, num_ranks: int, capacity: int, t_blk: float) -> float:
+    """t_c = t_blk * sum_i (s_i / (N C))^2 for a pack on a ring of N ranks."""
+    import numpy as np
+
+    a = np.ascontiguousarray(lengths, dtype=np.int32)
+    out = ctypes.c_double()
+    _check(load().hdp_ring_step_compute(a.ctypes.data_as(ctypes.c_void_p), int(a.size), int(num_ranks),
+                                        int(capacity), float(t_blk), ctypes.byref(out)), "hdp_ring_step_compute")
+    return out.value
+
+
+def hdp_ring_attention_time(num_ranks: int, t_c: float, t_x: float) -> float:
+    """T_attn = (N - 1) * max(t_c, t_x) + t_c."""
+    out = ctypes.c_double()
+    _check(load().hdp_ring_attention_time(int(num_ranks), float(t_c), float(t_x), ctypes.byref(out)),
+           "hdp_ring_attention_time")
+    return out.value
+
+
+def hdp_offload_ranks(model: dict, s: int, capacity: int):
+    """Eq. 3: (offload ratio r, rank count D) for a sequence of s tokens."""
+    m = OffloadModel(**{k: model[k] for k in ("alpha1", "beta1", "gamma", "alpha2", "beta2", "bw_d2h", "bw_h2d",
+                                              "layers")})
+    r, d = ctypes.c_double(), ctypes.c_int64()
+    _check(load().hdp_offload_ranks(ctypes.byref(m), int(s), int(capacity), ctypes.byref(r), ctypes.byref(d)),
+           "hdp_offload_ranks")
+    return r.value, int(d.value)
+
+
+def hdp_fit_cost_model(x, y, degree: int):
+    """Least-squares polynomial coefficients (of x^0 .. x^degree) through (x, y)."""
+    import numpy as np
+
+    xa = np.ascontiguousarray(x, dtype=np.float64)
+    ya = np.ascontiguousarray(y, dtype=np.float64)
+    if xa.shape != ya.shape:
+        raise ValueError("x and y differ in length")
+    coef = np.zeros(int(degree) + 1, dtype=np.float64)
+    _check(load().hdp_fit_cost_model(xa.ctypes.data_as(ctypes.c_void_p), ya.ctypes.data_as(ctypes.c_void_p),
+                                     int(xa.size), int(degree), coef.ctypes.data_as(ctypes.c_void_p)),
+           "hdp_fit_cost_model")
+    return coef

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhdpattn.so")
-SOURCES = ["api.cu", "plan.cu", "attn_fwd.cu", "lse_merge.cu"]
+SOURCES = ["api.cu", "plan.cu", "attn_fwd.cu", "lse_merge.cu", "cost_model.cpp"]
 HEADERS = ["internal.h", "sm103_ptx.cuh"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
@@ -43,7 +43,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     exe = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = [exe] + NVCC_FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
