@@ -486,7 +486,8 @@ def cost_model_mode(args):
     """Calibrates the cost models of the research digest (sections 3.2-3.3) on
     this GPU: times the attention of one document of s tokens (Hq = 32,
     Hkv = 8, d = 128, FUSED) for several s, fits T(s) = alpha1 s^2 + beta1 s +
-    gamma with the library's hdp_fit_cost_model, and derives the time of one
+    gamma with the library's hdp_fit_cost_model (weights 1/T^2: relative
+    error, the times span five orders of magnitude), and derives the time of one
     full C x C block, t_blk = 2 alpha1 C^2 (a causal document of s tokens has
     about s^2/2 query-key pairs, a full block C^2).  It then applies the ring
     model (hdp_ring_step_compute / hdp_ring_attention_time) with this t_blk
@@ -529,7 +530,7 @@ def cost_model_mode(args):
         del q, k, v, o, lse
     x = [p["s"] for p in points]
     y = [p["ms"] for p in points]
-    coef = pkg.hdp_fit_cost_model(x, y, 2)
+    coef = pkg.hdp_fit_cost_model(x, y, 2, w=[1.0 / (t * t) for t in y])  # relative errors
     alpha1, beta1, gamma = float(coef[2]), float(coef[1]), float(coef[0])
     t_blk = 2.0 * alpha1 * C * C
     t_x = 1.5
@@ -554,6 +555,53 @@ def cost_model_mode(args):
     return 0
 
 
+def balance_mode(args):
+    """Balance scheduler (research digest, section 3.4) on the 1M-token skewed
+    mixture: plan and per-shard FLOPs on the GPU (hdp_plan_create,
+    hdp_flops_per_shard), then hdp_balance_schedule on the host for several
+    worker counts.  Reports each schedule's slowest-worker load over the mean
+    (1.0 = perfect) for equal micro-batch counts (an infinite threshold),
+    DP-Balance (delta = 0, 4 buckets) and PP-Balance, and the host time of
+    one call.  One JSON line."""
+    import time
+
+    import numpy as np
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import build as native_build
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    w = wl.workload("mix1m", args.seed)
+    dl = torch.tensor(w.lengths, dtype=torch.int32, device="cuda")
+    plan = pkg.hdp_plan_create(dl, w.capacity)
+    flops = torch.empty(plan.view.num_shards, dtype=torch.int64, device="cuda")
+    pkg.hdp_flops_per_shard(plan, w.d, w.hq, flops)
+    costs = flops.cpu().numpy()
+    pkg.hdp_device_status()
+    plan.destroy()
+    rows = []
+    for R in (8, 16, 32, 64):
+        res = {"workers": R}
+        for label, delta, mode in (("equal_counts", (1 << 62), pkg.HDP_BALANCE_DP), ("dp_balance", 0,
+                                   pkg.HDP_BALANCE_DP), ("pp_balance", 0, pkg.HDP_BALANCE_PP)):
+            t0 = time.perf_counter()
+            reps = 20
+            for _ in range(reps):
+                _, load, _ = pkg.hdp_balance_schedule(costs, R, 4, delta, mode)
+            us = (time.perf_counter() - t0) / reps * 1e6
+            res[label] = {"max_over_mean": float(load.max() / load.mean()), "host_us_per_call": us}
+        rows.append(res)
+    out = {"mode": "balance", "workload": f"mix1m seed {args.seed}: {len(w.lengths)} sequences, "
+           f"{len(costs)} micro-batches of C = {w.capacity} tokens", "cost": "useful FLOPs per micro-batch "
+           "(hdp_flops_per_shard)", "max_over_mean_micro_batch_flops": float(costs.max() / costs.mean()),
+           "schedules": rows}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -568,6 +616,8 @@ def main():
     ap.add_argument("--kernels", action="store_true", help="time the plan stress input and the LSE merge")
     ap.add_argument("--cost-model", action="store_true",
                     help="calibrate T(s) and t_blk on this GPU and apply the ring model")
+    ap.add_argument("--balance", action="store_true",
+                    help="balance scheduler on the per-shard FLOPs of the 1M-token mixture")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -576,6 +626,8 @@ def main():
         return kernels_mode(args) if rank == 0 else 0
     if args.cost_model:
         return cost_model_mode(args) if rank == 0 else 0
+    if args.balance:
+        return balance_mode(args) if rank == 0 else 0
     if args.impl == "reference":
         return reference_arm(args, rank)
     return our_arm(args, ws, rank, local)

@@ -275,10 +275,43 @@ hdp_status_t hdp_offload_ranks(const hdp_offload_model_t* model, int64_t s, int6
 /*
  * Least-squares fit of a profiled cost model (section 3.3): the polynomial of
  * the given degree (1: Act(s) = c1 s + c0; 2: T(s) = c2 s^2 + c1 s + c0)
- * through n points (x_i, y_i); coef[k] is the coefficient of x^k.  n > degree
- * and at least degree + 1 distinct x values; coef has degree + 1 entries.
+ * minimising sum_i w_i (y_i - p(x_i))^2 over n points; coef[k] is the
+ * coefficient of x^k.  w: host double[n] of weights >= 0, or NULL for all
+ * ones (w_i = 1 / y_i^2 fits relative errors, for times spanning several
+ * orders of magnitude).  n > degree and at least degree + 1 distinct x values
+ * with positive weight; coef has degree + 1 entries.
  */
-hdp_status_t hdp_fit_cost_model(const double* x, const double* y, int32_t n, int32_t degree, double* coef);
+hdp_status_t hdp_fit_cost_model(const double* x, const double* y, const double* w, int32_t n, int32_t degree,
+                                double* coef);
+
+/* ====================================================================== */
+/* Balance scheduler (host arithmetic only).  Research digest, section 3.4 and
+ * Figure 4: micro-batches hold equal tokens but unequal attention FLOPs, so
+ * workers run different numbers of them.  The section states the steps but
+ * not Algorithm 2's text; the reading implemented here:
+ *   1. order the micro-batches by cost, heaviest first (ties: lower index);
+ *   2. cut that order into `buckets` consecutive buckets of about equal cost:
+ *      the item at sorted position p goes to bucket
+ *      min(B - 1, floor(B * P_p / total)), P_p the cost before it;
+ *   3. HDP_BALANCE_DP: workers draw from the front of the order (the first
+ *      non-empty bucket).  Each pass, every worker whose load trails the
+ *      slowest worker's by more than `delta` (load + delta < max load) takes
+ *      the next micro-batch, in worker order; when none trails, every worker
+ *      takes one.
+ *      HDP_BALANCE_PP: one bucket per pipeline (`buckets` is ignored and
+ *      taken as `workers`); pipeline p runs bucket p.
+ * costs: host int64[m] >= 0 (e.g. hdp_flops_per_shard copied to the host);
+ * worker_of_item: host int32[m] out; worker_load: host int64[workers] out;
+ * bucket_of_item: host int32[m] out, or NULL.  m >= 0, workers >= 1,
+ * buckets >= 1, delta >= 0.  Time O(m log m + passes * workers); uses a
+ * scratch array of m int32 allocated and freed inside the call
+ * (HDP_ERR_OUT_OF_MEMORY if that fails).  The sum of the costs must fit in
+ * int64. */
+#define HDP_BALANCE_DP 0
+#define HDP_BALANCE_PP 1
+hdp_status_t hdp_balance_schedule(const int64_t* costs, int32_t m, int32_t workers, int32_t buckets, int64_t delta,
+                                  int32_t mode, int32_t* worker_of_item, int64_t* worker_load,
+                                  int32_t* bucket_of_item);
 
 #ifdef __cplusplus
 }

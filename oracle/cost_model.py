@@ -80,15 +80,18 @@ def offload_ranks(model: dict, s: int, capacity: int):
     return float(r), int(d)
 
 
-def fit_cost_model(x, y, degree: int) -> np.ndarray:
-    """Least-squares polynomial through the points (the profiled cost models of
-    section 3.3 are fitted this way); coefficients of x^0 .. x^degree.  The
-    solve is numpy's least-squares routine on the Vandermonde matrix."""
+def fit_cost_model(x, y, degree: int, w=None) -> np.ndarray:
+    """Weighted least-squares polynomial through the points (the profiled cost
+    models of section 3.3 are fitted this way): minimise sum w_i (y_i - p(x_i))^2;
+    coefficients of x^0 .. x^degree.  The solve is numpy's least-squares
+    routine on the Vandermonde matrix with rows scaled by sqrt(w_i)."""
     x = np.asarray(x, dtype=np.float64)
     y = np.asarray(y, dtype=np.float64)
+    w = np.ones_like(x) if w is None else np.asarray(w, dtype=np.float64)
     # change of variable u = x / scale (same minimiser, better conditioned);
     # the coefficient of u^k is the coefficient of x^k times scale^k
-    scale = float(np.max(np.abs(x)))
-    v = np.vander(x / scale, degree + 1, increasing=True)
-    coef_u, *_ = np.linalg.lstsq(v, y, rcond=None)
+    scale = float(np.max(np.abs(x[w > 0])))
+    sw = np.sqrt(w)
+    v = np.vander(x / scale, degree + 1, increasing=True) * sw[:, None]
+    coef_u, *_ = np.linalg.lstsq(v, y * sw, rcond=None)
     return coef_u / scale ** np.arange(degree + 1)

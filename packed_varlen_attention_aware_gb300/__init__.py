@@ -13,6 +13,8 @@ import math
 
 from .binding import (  # noqa: F401
     EXPORTED,
+    HDP_BALANCE_DP,
+    HDP_BALANCE_PP,
     HDP_ERR_CUDA,
     HDP_ERR_DEVICE_TIMEOUT,
     HDP_ERR_INVALID_ARGUMENT,
@@ -28,6 +30,7 @@ from .binding import (  # noqa: F401
     Plan,
     hdp_attention_fwd,
     hdp_attention_fwd_split_noalloc,
+    hdp_balance_schedule,
     hdp_attention_workspace_bytes,
     hdp_device_status,
     hdp_fit_cost_model,

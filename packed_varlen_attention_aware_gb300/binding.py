@@ -23,6 +23,8 @@ HDP_MODE_FUSED = 0
 HDP_MODE_SPLIT = 1
 HDP_PLAN_DEFAULT = 0
 HDP_PLAN_NO_SHARDS = 1
+HDP_BALANCE_DP = 0
+HDP_BALANCE_PP = 1
 
 # Every symbol include/hdpattn.h declares.
 EXPORTED = (
@@ -31,6 +33,7 @@ EXPORTED = (
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
     "hdp_kernel_launch_count", "hdp_attention_fwd_split_noalloc",
     "hdp_ring_step_compute", "hdp_ring_attention_time", "hdp_offload_ranks", "hdp_fit_cost_model",
+    "hdp_balance_schedule",
 )
 
 
@@ -93,7 +96,8 @@ def load(path: str | None = None):
             "hdp_ring_attention_time": [I32, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
             "hdp_offload_ranks": [ctypes.POINTER(OffloadModel), I64, I64, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(I64)],
-            "hdp_fit_cost_model": [V, V, I32, I32, V],
+            "hdp_fit_cost_model": [V, V, V, I32, I32, V],
+            "hdp_balance_schedule": [V, I32, I32, I32, I64, I32, V, V, V],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -303,16 +307,42 @@ def hdp_offload_ranks(model: dict, s: int, capacity: int):
     return r.value, int(d.value)
 
 
-def hdp_fit_cost_model(x, y, degree: int):
-    """Least-squares polynomial coefficients (of x^0 .. x^degree) through (x, y)."""
+def hdp_fit_cost_model(x, y, degree: int, w=None):
+    """Weighted least-squares polynomial coefficients (of x^0 .. x^degree)
+    through (x, y); w None = unweighted."""
     import numpy as np
 
     xa = np.ascontiguousarray(x, dtype=np.float64)
     ya = np.ascontiguousarray(y, dtype=np.float64)
     if xa.shape != ya.shape:
         raise ValueError("x and y differ in length")
+    wa = None if w is None else np.ascontiguousarray(w, dtype=np.float64)
+    if wa is not None and wa.shape != xa.shape:
+        raise ValueError("w and x differ in length")
     coef = np.zeros(int(degree) + 1, dtype=np.float64)
-    _check(load().hdp_fit_cost_model(xa.ctypes.data_as(ctypes.c_void_p), ya.ctypes.data_as(ctypes.c_void_p),
-                                     int(xa.size), int(degree), coef.ctypes.data_as(ctypes.c_void_p)),
+    vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    _check(load().hdp_fit_cost_model(vp(xa), vp(ya), vp(wa), int(xa.size), int(degree), vp(coef)),
            "hdp_fit_cost_model")
     return coef
+
+
+# ---------------------------------------------------------------- balance scheduler (host)
+
+def hdp_balance_schedule(costs, workers: int, buckets: int, delta: int, mode: int = HDP_BALANCE_DP):
+    """Section 3.4 balance scheduler.  Returns numpy arrays
+    (worker of each micro-batch int32[m], load of each worker int64[workers],
+    bucket of each micro-batch int32[m])."""
+    import numpy as np
+
+    c = np.ascontiguousarray(costs, dtype=np.int64)
+    m = int(c.size)
+    w = np.empty(m, dtype=np.int32)
+    load = np.empty(int(workers), dtype=np.int64)
+    b = np.empty(m, dtype=np.int32)
+    vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(load_lib().hdp_balance_schedule(vp(c), m, int(workers), int(buckets), int(delta), int(mode), vp(w),
+                                           vp(load), vp(b)), "hdp_balance_schedule")
+    return w, load, b
+
+
+load_lib = load

@@ -116,22 +116,24 @@ hdp_status_t hdp_offload_ranks(const hdp_offload_model_t* m, int64_t s, int64_t 
   return HDP_OK;
 }
 
-hdp_status_t hdp_fit_cost_model(const double* x, const double* y, int32_t n, int32_t degree, double* coef) {
+hdp_status_t hdp_fit_cost_model(const double* x, const double* y, const double* w, int32_t n, int32_t degree,
+                                double* coef) {
   if (!x || !y || !coef) return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: null pointer");
   if (degree < 1 || degree > 2 || n <= degree)
     return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: degree 1 or 2 and n > degree");
   double scale = 0;
   for (int32_t i = 0; i < n; ++i) {
-    if (!std::isfinite(x[i]) || !std::isfinite(y[i]))
-      return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: non-finite point");
-    scale = std::fmax(scale, std::fabs(x[i]));
+    if (!std::isfinite(x[i]) || !std::isfinite(y[i]) || (w && !(w[i] >= 0.0 && std::isfinite(w[i]))))
+      return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: non-finite point or negative weight");
+    if (!w || w[i] > 0) scale = std::fmax(scale, std::fabs(x[i]));
   }
-  if (scale == 0) return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: all x are zero");
-  // at least degree + 1 distinct x values
+  if (scale == 0) return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: all weighted x are zero");
+  // at least degree + 1 distinct x values with positive weight
   {
-    double seen[2] = {x[0], x[0]};
-    int distinct = 1;
-    for (int32_t i = 1; i < n && distinct <= degree; ++i) {
+    double seen[2] = {0, 0};
+    int distinct = 0;
+    for (int32_t i = 0; i < n && distinct <= degree; ++i) {
+      if (w && !(w[i] > 0)) continue;
       bool fresh = true;
       for (int k = 0; k < distinct; ++k) fresh = fresh && x[i] != seen[k];
       if (fresh) {
@@ -142,15 +144,17 @@ hdp_status_t hdp_fit_cost_model(const double* x, const double* y, int32_t n, int
     if (distinct <= degree)
       return hdp::fail(HDP_ERR_INVALID_ARGUMENT, "hdp_fit_cost_model: fewer than degree + 1 distinct x values");
   }
-  // normal equations in u = x / scale, accumulated in long double
+  // weighted normal equations in u = x / scale, accumulated in long double
   const int m = degree + 1;
   long double ata[9] = {0}, aty[3] = {0};
   for (int32_t i = 0; i < n; ++i) {
+    const long double wi = w ? w[i] : 1.0;
+    if (!(wi > 0)) continue;
     const long double u = static_cast<long double>(x[i]) / scale;
     long double p[3] = {1, u, u * u};
     for (int r = 0; r < m; ++r) {
-      aty[r] += p[r] * y[i];
-      for (int c = 0; c < m; ++c) ata[r * m + c] += p[r] * p[c];
+      aty[r] += wi * p[r] * y[i];
+      for (int c = 0; c < m; ++c) ata[r * m + c] += wi * p[r] * p[c];
     }
   }
   double a[9], b[3];

@@ -78,8 +78,9 @@ def test_fit_matches_oracle(degree):
         x = rng.uniform(256, 2_097_152, n)
         coef_true = [rng.uniform(0, 1), rng.uniform(0, 1e-4), rng.uniform(0, 1e-9)][: degree + 1]
         y = sum(c * x**k for k, c in enumerate(coef_true)) * (1 + rng.normal(0, 0.01, n))
-        got = pkg.hdp_fit_cost_model(x, y, degree)
-        ref = cm.fit_cost_model(x, y, degree)
+        w = None if _ % 2 else rng.uniform(0, 2, n) / np.maximum(y, 1e-30) ** 2
+        got = pkg.hdp_fit_cost_model(x, y, degree, w)
+        ref = cm.fit_cost_model(x, y, degree, w)
         # compare the fitted curves over the sampled range (coefficients of an
         # ill-conditioned basis can differ more than the curves do)
         xs = np.linspace(x.min(), x.max(), 64)
@@ -113,3 +114,7 @@ def test_argument_errors():
         pkg.hdp_fit_cost_model([1.0, 2.0], [1.0, 2.0], 2)             # n <= degree
     with pytest.raises(E):
         pkg.hdp_fit_cost_model([1.0, 2.0, math.nan], [1.0, 2.0, 3.0], 1)
+    with pytest.raises(E):
+        pkg.hdp_fit_cost_model([1.0, 2.0, 3.0], [1.0, 2.0, 3.0], 1, w=[1.0, -1.0, 1.0])
+    with pytest.raises(E):
+        pkg.hdp_fit_cost_model([1.0, 2.0, 3.0], [1.0, 2.0, 3.0], 1, w=[1.0, 0.0, 0.0])  # one weighted x

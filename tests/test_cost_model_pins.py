@@ -150,3 +150,23 @@ def test_fit_satisfies_normal_equations():
     v = np.vander(x, 3, increasing=True)
     resid = y - v @ coef
     assert np.max(np.abs(v.T @ resid)) <= 1e-8 * np.max(np.abs(v.T @ y))
+
+
+def test_weighted_fit_recovers_and_satisfies_weighted_normal_equations():
+    x = np.array([2048, 4096, 8192, 16384, 32768, 65536, 131072], dtype=np.float64)
+    y = 4e-9 * x**2 + 2e-5 * x + 0.05
+    w = 1.0 / y**2
+    coef = cm.fit_cost_model(x, y, 2, w)
+    assert np.allclose(coef, [0.05, 2e-5, 4e-9], rtol=1e-7, atol=0)
+    rng = np.random.default_rng(9)
+    yn = y * (1 + rng.normal(0, 0.05, x.size))
+    coef = cm.fit_cost_model(x, yn, 2, w)
+    v = np.vander(x, 3, increasing=True)
+    g = v.T @ (w * (yn - v @ coef))
+    assert np.all(np.abs(g) <= 1e-8 * (v.T @ (w * np.abs(yn))))
+    # a zero weight removes a point: same fit as without it
+    w2 = w.copy()
+    w2[3] = 0.0
+    keep = np.arange(x.size) != 3
+    assert np.allclose(cm.fit_cost_model(x, yn, 2, w2), cm.fit_cost_model(x[keep], yn[keep], 2, w[keep]),
+                       rtol=1e-9, atol=0)
