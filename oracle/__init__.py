@@ -17,6 +17,10 @@ from .oracle import (  # noqa: F401
     plan_sizes,
     attention,
     attention_rows,
+    attention_f64,
+    attention_bwd,
+    attention_bwd_dq_rows,
+    bf16_bits_to_f64,
     merge,
     flops_total,
     flops_per_shard,

@@ -410,3 +410,185 @@ int oracle_merge(int32_t m, int64_t rows, int32_t d, const double* o_parts, cons
   }
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ backward */
+
+/*
+ * The training step the pages time runs a forward and a backward pass over
+ * the same packed micro-batch (review and digest, section 5: forward plus
+ * backward bars).  The backward of document-masked causal attention is the
+ * gradient of L = sum_{t,h,c} O[t][h][c] dO[t][h][c] with respect to q, k, v,
+ * written out from its definition.  For query row a of query head h (kv head
+ * g = h / (hq/hkv)) and the keys b <= a of a's own document:
+ *   S_ab  = scale q_a . k_b
+ *   P_ab  = exp(S_ab - lse_a),  lse_a = ln sum_b exp(S_ab)     (two passes)
+ *   dP_ab = dO_a . v_b
+ *   Dl_a  = sum_b P_ab dP_ab
+ *   dS_ab = P_ab (dP_ab - Dl_a)
+ *   dq_a  = scale sum_b dS_ab k_b
+ *   dk_b += scale dS_ab q_a        (summed over the query heads of g)
+ *   dv_b += P_ab dO_a              (summed over the query heads of g)
+ * Inputs and outputs are fp64 so that finite differences of the forward
+ * below can pin it; callers with bf16 data convert exactly.
+ */
+
+/* Forward on fp64 inputs (same definition as oracle_attention). */
+int oracle_attention_f64(const double* q, const double* k, const double* v, const int32_t* cu_seqlens, int32_t n,
+                         int32_t hq, int32_t hkv, int32_t d, double scale, double* o, double* lse) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  const int32_t grp = hq / hkv;
+  for (int64_t t = 0; t < T; t++) {
+    const int32_t i = doc_of_token(cu_seqlens, n, t);
+    const int64_t start = cu_seqlens[i];
+    for (int32_t h = 0; h < hq; h++) {
+      const int32_t g = h / grp;
+      const double* qa = q + (t * hq + h) * (int64_t)d;
+      double m = -INFINITY;
+      for (int64_t b = start; b <= t; b++) {
+        double s = 0.0;
+        for (int32_t c = 0; c < d; c++) s += qa[c] * k[(b * hkv + g) * (int64_t)d + c];
+        s *= scale;
+        if (s > m) m = s;
+      }
+      double sum = 0.0;
+      for (int64_t b = start; b <= t; b++) {
+        double s = 0.0;
+        for (int32_t c = 0; c < d; c++) s += qa[c] * k[(b * hkv + g) * (int64_t)d + c];
+        sum += exp(s * scale - m);
+      }
+      const double L = m + log(sum);
+      double* oa = o + (t * hq + h) * (int64_t)d;
+      for (int32_t c = 0; c < d; c++) oa[c] = 0.0;
+      for (int64_t b = start; b <= t; b++) {
+        double s = 0.0;
+        for (int32_t c = 0; c < d; c++) s += qa[c] * k[(b * hkv + g) * (int64_t)d + c];
+        const double p = exp(s * scale - L);
+        for (int32_t c = 0; c < d; c++) oa[c] += p * v[(b * hkv + g) * (int64_t)d + c];
+      }
+      lse[(int64_t)h * T + t] = L;
+    }
+  }
+  return ORC_OK;
+}
+
+/* One query row of the backward: fills P (probabilities) and dS for keys
+ * b = start..a, accumulates dq_a.  p and ds have room for a - start + 1. */
+static void bwd_row(const double* q, const double* k, const double* v, const double* dout, int32_t hq, int32_t hkv,
+                    int32_t d, double scale, int64_t start, int64_t a, int32_t h, double* p, double* ds,
+                    double* dq_a) {
+  const int32_t g = h / (hq / hkv);
+  const double* qa = q + (a * hq + h) * (int64_t)d;
+  const double* doa = dout + (a * hq + h) * (int64_t)d;
+  const int64_t nk = a - start + 1;
+  double m = -INFINITY;
+  for (int64_t j = 0; j < nk; j++) {
+    const double* kb = k + ((start + j) * hkv + g) * (int64_t)d;
+    double s = 0.0;
+    for (int32_t c = 0; c < d; c++) s += qa[c] * kb[c];
+    p[j] = s * scale;
+    if (p[j] > m) m = p[j];
+  }
+  double sum = 0.0;
+  for (int64_t j = 0; j < nk; j++) sum += exp(p[j] - m);
+  const double L = m + log(sum);
+  double dl = 0.0;
+  for (int64_t j = 0; j < nk; j++) {
+    p[j] = exp(p[j] - L);
+    const double* vb = v + ((start + j) * hkv + g) * (int64_t)d;
+    double dp = 0.0;
+    for (int32_t c = 0; c < d; c++) dp += doa[c] * vb[c];
+    ds[j] = dp;
+    dl += p[j] * dp;
+  }
+  for (int32_t c = 0; c < d; c++) dq_a[c] = 0.0;
+  for (int64_t j = 0; j < nk; j++) {
+    ds[j] = p[j] * (ds[j] - dl);
+    const double* kb = k + ((start + j) * hkv + g) * (int64_t)d;
+    for (int32_t c = 0; c < d; c++) dq_a[c] += scale * ds[j] * kb[c];
+  }
+}
+
+/* Full backward.  dq [T][hq][d], dk and dv [T][hkv][d], all fp64. */
+int oracle_attention_bwd(const double* q, const double* k, const double* v, const double* dout,
+                         const int32_t* cu_seqlens, int32_t n, int32_t hq, int32_t hkv, int32_t d, double scale,
+                         double* dq, double* dk, double* dv) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  const int32_t grp = hq / hkv;
+  memset(dk, 0, sizeof(double) * (size_t)(T * hkv * d));
+  memset(dv, 0, sizeof(double) * (size_t)(T * hkv * d));
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; i++)
+    if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen) maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+  int err = ORC_OK;
+  /* one (document, kv head) per iteration: its dk/dv rows and the dq rows of
+   * its query heads are written by that iteration alone */
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    double* ds = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!p || !ds) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t w = 0; w < (int64_t)n * hkv; w++) {
+        const int32_t i = (int32_t)(w / hkv), g = (int32_t)(w % hkv);
+        const int64_t start = cu_seqlens[i], end = cu_seqlens[i + 1];
+        for (int32_t h = g * grp; h < (g + 1) * grp; h++) {
+          for (int64_t a = start; a < end; a++) {
+            bwd_row(q, k, v, dout, hq, hkv, d, scale, start, a, h, p, ds, dq + (a * hq + h) * (int64_t)d);
+            const double* qa = q + (a * hq + h) * (int64_t)d;
+            const double* doa = dout + (a * hq + h) * (int64_t)d;
+            for (int64_t j = 0; j <= a - start; j++) {
+              double* dkb = dk + ((start + j) * hkv + g) * (int64_t)d;
+              double* dvb = dv + ((start + j) * hkv + g) * (int64_t)d;
+              for (int32_t c = 0; c < d; c++) {
+                dkb[c] += scale * ds[j] * qa[c];
+                dvb[c] += p[j] * doa[c];
+              }
+            }
+          }
+        }
+      }
+    }
+    free(p);
+    free(ds);
+  }
+  return err;
+}
+
+/* Sampled dq rows: dq_out[i] = dq of token tokens[i], query head heads[i]. */
+int oracle_attention_bwd_dq_rows(const double* q, const double* k, const double* v, const double* dout,
+                                 const int32_t* cu_seqlens, int32_t n, int32_t hq, int32_t hkv, int32_t d,
+                                 double scale, const int64_t* tokens, const int32_t* heads, int64_t ns,
+                                 double* dq_out) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; i++)
+    if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen) maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+  for (int64_t i = 0; i < ns; i++)
+    if (tokens[i] < 0 || tokens[i] >= T || heads[i] < 0 || heads[i] >= hq) return ORC_EINVAL;
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    double* ds = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!p || !ds) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t i = 0; i < ns; i++) {
+        const int32_t doc = doc_of_token(cu_seqlens, n, tokens[i]);
+        bwd_row(q, k, v, dout, hq, hkv, d, scale, cu_seqlens[doc], tokens[i], heads[i], p, ds,
+                dq_out + i * (int64_t)d);
+      }
+    }
+    free(p);
+    free(ds);
+  }
+  return err;
+}

@@ -49,6 +49,9 @@ def _load():
             lib.oracle_attention.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P]
             lib.oracle_attention_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P, P, P, i64, P, P]
             lib.oracle_merge.argtypes = [i32, i64, i32, P, P, P, P]
+            lib.oracle_attention_f64.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P]
+            lib.oracle_attention_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, P]
+            lib.oracle_attention_bwd_dq_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, i64, P]
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -171,6 +174,67 @@ def attention_rows(q, k, v, cu_seqlens, hq: int, hkv: int, d: int, scale: float,
     if rc != 0:
         raise ValueError(f"oracle_attention_rows failed (rc={rc})")
     return o, lse
+
+
+def bf16_bits_to_f64(x: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns -> float64, exactly."""
+    x = _bits(x)
+    return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _f64(x) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return bf16_bits_to_f64(x)
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def attention_f64(q, k, v, cu_seqlens, hq: int, hkv: int, d: int, scale: float):
+    """Forward on fp64 inputs (or bf16 bit patterns, converted exactly).
+    Returns o [T][hq][d] and lse [hq][T] in fp64."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    T = int(cu[-1])
+    o = np.zeros((T, hq, d), np.float64)
+    lse = np.zeros((hq, T), np.float64)
+    rc = lib.oracle_attention_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, hq, hkv, d, float(scale),
+                                  _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_f64 failed (rc={rc})")
+    return o, lse
+
+
+def attention_bwd(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int, scale: float):
+    """Gradients of sum(O * dout) w.r.t. q, k, v (fp64; bf16 inputs converted
+    exactly).  Returns dq [T][hq][d], dk [T][hkv][d], dv [T][hkv][d]."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    T = int(cu[-1])
+    dq = np.zeros((T, hq, d), np.float64)
+    dk = np.zeros((T, hkv, d), np.float64)
+    dv = np.zeros((T, hkv, d), np.float64)
+    rc = lib.oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(cu), len(cu) - 1, hq, hkv, d,
+                                  float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd failed (rc={rc})")
+    return dq, dk, dv
+
+
+def attention_bwd_dq_rows(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int, scale: float, tokens, heads):
+    """dq of sampled (token, query head) rows, fp64 [ns][d]."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    t = np.ascontiguousarray(tokens, np.int64)
+    h = np.ascontiguousarray(heads, np.int32)
+    out = np.zeros((len(t), d), np.float64)
+    rc = lib.oracle_attention_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(cu), len(cu) - 1, hq, hkv, d,
+                                          float(scale), _ptr(t), _ptr(h), len(t), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dq_rows failed (rc={rc})")
+    return out
 
 
 def merge(o_parts, lse_parts):
