@@ -87,8 +87,12 @@ typedef struct {
   const int32_t* shard_of_chunk; /* [N_c] shard of each chunk (NULL if skipped) */
   /* Query-tile work lists, heaviest first (weight descending, then
    * enumeration order).  Rows of 8 int32: {q_row0, q_rows, kv_row0, kv_len,
-   * block (-1 in the fused list), row offset inside the query chunk, weight =
-   * key tiles, 0}.  Fully masked (cross-document or future) tiles never appear. */
+   * block (-1 in the fused list), row offset of the tile inside its query
+   * chunk (inside its document in the fused list), weight = key tiles,
+   * document length (fused list; 0 in the split list)}.  Fully masked
+   * (cross-document or future) tiles never appear.  In the fused list the
+   * rows of query tile j of a document also describe its key tile j (same
+   * rows), which the backward pass walks. */
   const int32_t* tiles_fused;    /* [num_tiles_fused][8] one per document query tile */
   int64_t num_tiles_fused;
   const int32_t* tiles_split;    /* [num_tiles_split][8] one per block query tile
@@ -174,6 +178,26 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
 hdp_status_t hdp_attention_fwd_split_noalloc(hdp_plan_t plan, const void* q, const void* k, const void* v,
                                              int32_t hq, int32_t hkv, int32_t d, float scale, void* o, float* lse,
                                              void* stream);
+
+/*
+ * Backward pass of the same attention (the training step of section 5 times
+ * forward and backward together; each document's gradient is independent,
+ * section 3.2).  With P = exp(scale Q K^T - lse) over the causal keys of each
+ * query's own document and D = rowsum(dout * o):
+ *   dv = P^T dout,  dS = P * (dout V^T - D),  dk = scale dS^T Q,  dq = scale dS K
+ * summed over the query heads of each GQA group for dk and dv.
+ *   q, o, dout, dq: [T][hq][d] bf16;  k, v, dk, dv: [T][hkv][d] bf16;
+ *   lse: [hq][T] fp32, natural log, as written by hdp_attention_fwd for this
+ *   plan (FUSED or SPLIT) and `o` its output.
+ * workspace: device, 256-byte aligned, at least
+ * hdp_attention_bwd_workspace_bytes (an fp32 dq accumulator and D).
+ * d == 64 or 128 (UNSUPPORTED otherwise); tensor pointers 16-byte aligned.
+ * Every output row is written.
+ */
+hdp_status_t hdp_attention_bwd_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t d, size_t* bytes);
+hdp_status_t hdp_attention_bwd(hdp_plan_t plan, const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, int32_t hq, int32_t hkv, int32_t d, float scale,
+                               void* workspace, size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream);
 
 /*
  * Exact log-sum-exp merge of the causal blocks of every query chunk

@@ -20,6 +20,7 @@ from .oracle import (  # noqa: F401
     attention_f64,
     attention_bwd,
     attention_bwd_dq_rows,
+    attention_bwd_dkv_rows,
     bf16_bits_to_f64,
     merge,
     flops_total,

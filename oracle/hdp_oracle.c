@@ -592,3 +592,58 @@ int oracle_attention_bwd_dq_rows(const double* q, const double* k, const double*
   }
   return err;
 }
+
+/* Sampled dk / dv rows: key token tokens[i] of kv head kv_heads[i]; sums over
+ * the query heads of that group and the queries a >= the key in its document.
+ * dk_out, dv_out [ns][d].  Cost per sample: (group x later queries) rows of
+ * O(s d) each, so keys near the end of long documents are cheap. */
+int oracle_attention_bwd_dkv_rows(const double* q, const double* k, const double* v, const double* dout,
+                                  const int32_t* cu_seqlens, int32_t n, int32_t hq, int32_t hkv, int32_t d,
+                                  double scale, const int64_t* tokens, const int32_t* kv_heads, int64_t ns,
+                                  double* dk_out, double* dv_out) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1) return ORC_EINVAL;
+  const int64_t T = cu_seqlens[n];
+  const int32_t grp = hq / hkv;
+  int32_t maxlen = 0;
+  for (int32_t i = 0; i < n; i++)
+    if (cu_seqlens[i + 1] - cu_seqlens[i] > maxlen) maxlen = cu_seqlens[i + 1] - cu_seqlens[i];
+  for (int64_t i = 0; i < ns; i++)
+    if (tokens[i] < 0 || tokens[i] >= T || kv_heads[i] < 0 || kv_heads[i] >= hkv) return ORC_EINVAL;
+  int err = ORC_OK;
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    double* ds = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    double* dq_a = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!p || !ds || !dq_a) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t i = 0; i < ns; i++) {
+        const int64_t b = tokens[i];
+        const int32_t g = kv_heads[i];
+        const int32_t doc = doc_of_token(cu_seqlens, n, b);
+        const int64_t start = cu_seqlens[doc], end = cu_seqlens[doc + 1];
+        double* dkb = dk_out + i * (int64_t)d;
+        double* dvb = dv_out + i * (int64_t)d;
+        for (int32_t c = 0; c < d; c++) dkb[c] = dvb[c] = 0.0;
+        for (int32_t h = g * grp; h < (g + 1) * grp; h++) {
+          for (int64_t a = b; a < end; a++) {
+            bwd_row(q, k, v, dout, hq, hkv, d, scale, start, a, h, p, ds, dq_a);
+            const double* qa = q + (a * hq + h) * (int64_t)d;
+            const double* doa = dout + (a * hq + h) * (int64_t)d;
+            for (int32_t c = 0; c < d; c++) {
+              dkb[c] += scale * ds[b - start] * qa[c];
+              dvb[c] += p[b - start] * doa[c];
+            }
+          }
+        }
+      }
+    }
+    free(p);
+    free(ds);
+    free(dq_a);
+  }
+  return err;
+}

@@ -52,6 +52,7 @@ def _load():
             lib.oracle_attention_f64.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, P, P]
             lib.oracle_attention_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, P]
             lib.oracle_attention_bwd_dq_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, i64, P]
+            lib.oracle_attention_bwd_dkv_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, i64, P, P]
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -237,6 +238,23 @@ def attention_bwd_dq_rows(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int, 
     return out
 
 
+def attention_bwd_dkv_rows(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int, scale: float, tokens,
+                           kv_heads):
+    """dk and dv of sampled (key token, kv head) rows, fp64 [ns][d] each."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    t = np.ascontiguousarray(tokens, np.int64)
+    g = np.ascontiguousarray(kv_heads, np.int32)
+    dk = np.zeros((len(t), d), np.float64)
+    dv = np.zeros((len(t), d), np.float64)
+    rc = lib.oracle_attention_bwd_dkv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(cu), len(cu) - 1, hq, hkv, d,
+                                           float(scale), _ptr(t), _ptr(g), len(t), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dkv_rows failed (rc={rc})")
+    return dk, dv
+
+
 def merge(o_parts, lse_parts):
     """o_parts [m][rows][d], lse_parts [m][rows] -> (o [rows][d], lse [rows])."""
     lib = _load()
@@ -263,7 +281,8 @@ def tile_worklist(p: dict, tile: int = 128, split: bool = False) -> np.ndarray:
     enumeration order (doc / block ascending, query tile ascending).
 
     Each row: q_row0, q_rows, kv_row0, kv_len, block (-1 when not split),
-    row offset of the tile inside its query chunk, weight, 0.
+    row offset of the tile inside its query chunk (inside its document when
+    not split), weight, document length when not split (0 when split).
     """
     items = []
     ct = p["chunk_table"]
@@ -277,7 +296,7 @@ def tile_worklist(p: dict, tile: int = 128, split: bool = False) -> np.ndarray:
                 qrows = min(tile, s - qt * tile)
                 kv_len = qt * tile + qrows
                 w = (kv_len + tile - 1) // tile
-                items.append((q0, qrows, start, kv_len, -1, qt * tile, w, 0))
+                items.append((q0, qrows, start, kv_len, -1, qt * tile, w, s))
     else:
         for b, (qc, kc) in enumerate(p["block_table"]):
             qdoc, _, qbeg, qlen = (int(x) for x in ct[qc])

@@ -28,6 +28,8 @@ from .binding import (  # noqa: F401
     HdpError,
     OffloadModel,
     Plan,
+    hdp_attention_bwd,
+    hdp_attention_bwd_workspace_bytes,
     hdp_attention_fwd,
     hdp_attention_fwd_split_noalloc,
     hdp_balance_schedule,
@@ -72,3 +74,19 @@ def attention(q, k, v, d_lengths, capacity: int, mode: int = HDP_MODE_FUSED, sca
         ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     hdp_attention_fwd(plan, q, k, v, hq, hkv, d, scale, mode, ws, o, lse, stream=stream)
     return o, lse, plan
+
+
+def attention_backward(plan: Plan, q, k, v, o, lse, dout, scale: float | None = None, stream=None):
+    """Gradients (dq, dk, dv) of sum(o * dout) for the forward that produced
+    (o, lse) with this plan.  bf16 CUDA tensors in the forward's layouts."""
+    import torch
+
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = hdp_attention_bwd_workspace_bytes(plan, hq, d)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    hdp_attention_bwd(plan, q, k, v, o, lse, dout, hq, hkv, d, scale, ws, dq, dk, dv, stream=stream)
+    return dq, dk, dv

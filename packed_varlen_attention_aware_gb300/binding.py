@@ -33,7 +33,7 @@ EXPORTED = (
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
     "hdp_kernel_launch_count", "hdp_attention_fwd_split_noalloc",
     "hdp_ring_step_compute", "hdp_ring_attention_time", "hdp_offload_ranks", "hdp_fit_cost_model",
-    "hdp_balance_schedule",
+    "hdp_balance_schedule", "hdp_attention_bwd_workspace_bytes", "hdp_attention_bwd",
 )
 
 
@@ -98,6 +98,8 @@ def load(path: str | None = None):
                                   ctypes.POINTER(I64)],
             "hdp_fit_cost_model": [V, V, V, I32, I32, V],
             "hdp_balance_schedule": [V, I32, I32, I32, I64, I32, V, V, V],
+            "hdp_attention_bwd_workspace_bytes": [V, I32, I32, ctypes.POINTER(SZ)],
+            "hdp_attention_bwd": [V, V, V, V, V, V, V, I32, I32, I32, F32, V, SZ, V, V, V, V],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -243,6 +245,22 @@ def hdp_attention_fwd_split_noalloc(plan: Plan, q, k, v, hq: int, hkv: int, d: i
     _check(load().hdp_attention_fwd_split_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), hq, hkv, d, float(scale),
                                                   _ptr(o), _ptr(lse), _stream(stream)),
            "hdp_attention_fwd_split_noalloc")
+
+
+def hdp_attention_bwd_workspace_bytes(plan: Plan, hq: int, d: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().hdp_attention_bwd_workspace_bytes(plan.handle, hq, d, ctypes.byref(out)),
+           "hdp_attention_bwd_workspace_bytes")
+    return out.value
+
+
+def hdp_attention_bwd(plan: Plan, q, k, v, o, lse, dout, hq: int, hkv: int, d: int, scale: float, workspace, dq, dk,
+                      dv, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().hdp_attention_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), hq, hkv,
+                                    d, float(scale), _ptr(workspace), ws_bytes, _ptr(dq), _ptr(dk), _ptr(dv),
+                                    _stream(stream)),
+           "hdp_attention_bwd")
 
 
 def hdp_lse_merge(plan: Plan, o_part, lse_part, hq: int, d: int, o, lse, stream=None):

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhdpattn.so")
-SOURCES = ["api.cu", "plan.cu", "attn_fwd.cu", "lse_merge.cu", "cost_model.cpp", "balance.cpp"]
+SOURCES = ["api.cu", "plan.cu", "attn_fwd.cu", "attn_bwd.cu", "lse_merge.cu", "cost_model.cpp", "balance.cpp"]
 HEADERS = ["internal.h", "sm103_ptx.cuh"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 

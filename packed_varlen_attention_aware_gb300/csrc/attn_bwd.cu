@@ -1,0 +1,636 @@
+// Backward pass of document-masked causal attention on tcgen05 tensor cores.
+// The training step timed in "ByteScale: Communication-Efficient Scaling of
+// LLM Training with a 2048K Context Length on 16384 GPUs" (research digest,
+// section 5: forward and backward bars) runs this after the forward of the
+// same packed micro-batch; a query attends only to its own sequence
+// (section 3.2), so the gradient of every document is independent.
+//
+// With P = exp(scale Q K^T - LSE) (causal, same document), D = rowsum(dO * O):
+//   dV = P^T dO,  dS = P * (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Design (one persistent CTA per SM, 12 warps).  A work unit is one key tile
+// (128 keys of one document) for one key/value head; it walks every query
+// head of that head's GQA group and every query tile of the document from the
+// key tile's diagonal on, so fully masked tiles are never touched.  dK and dV
+// of the unit accumulate in TMEM for the whole unit; dQ of each query tile is
+// produced in TMEM and added into an fp32 workspace.
+//   warps 0-3  dS warps: thread = key row.  S^T and dP^T (keys on the TMEM
+//              lanes) -> P^T and dS^T in bf16, written back into TMEM for the
+//              dV / dK MMAs and dS into shared memory for the dQ MMA
+//   warps 4-7  dQ warps: thread = query row of the dQ tile -> vector atomic
+//              adds; at the end of a unit, dK and dV rows -> bf16 outputs
+//   warp 8     TMA producer        warp 9     MMA issuer + TMEM owner
+// Per query tile i of the unit (key tile j):
+//   S^T  = K_j Q_i^T      dP^T = V_j dO_i^T           (SS, M = keys)
+//   dV  += P^T dO_i       dK  += dS^T Q_i             (TS, A from TMEM)
+//   dQ_i  = dS K_j                                    (SS, A = dS in smem, MN-major)
+// TMEM (512 columns): dV [0,D) dK [D,2D) S^T [2D,2D+128) dP^T [2D+128,2D+256);
+// P^T aliases S^T's first 64 columns, dS^T and then dQ alias dP^T's.
+// Every wait is bounded; a timeout sets the device error word and all roles
+// stop at the same point, drain and free TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace hdp {
+
+hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, int heads, int d);
+
+namespace {
+
+constexpr int kBwdThreads = 384;
+constexpr int kBwdProducer = 8;
+constexpr int kBwdMma = 9;
+constexpr uint32_t kDsBarrier = 2;  // named barrier of the four dS warps
+
+constexpr int kErrBKv = 0x201, kErrBQ = 0x202, kErrBS = 0x203, kErrBP = 0x204, kErrBDq = 0x205,
+              kErrBDqE = 0x206, kErrBDkv = 0x207, kErrBDkvE = 0x208, kErrBKvE = 0x209, kErrBQE = 0x20a;
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTileBytes = kTile * D * 2;  // 128 x D bf16
+  static constexpr int kHalfBytes = kTile * 64 * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;           // 2 stages
+  static constexpr int kDO = kQ + 2 * kTileBytes;      // 2 stages
+  static constexpr int kDS = kDO + 2 * kTileBytes;     // 128 keys x 128 queries bf16, MN-major
+  static constexpr int kLse = kDS + kTile * kTile * 2; // 128 fp32: LSE * log2(e) of the tile's queries
+  static constexpr int kDl = kLse + kTile * 4;         // 128 fp32: D of the tile's queries
+  static constexpr int kBar = kDl + kTile * 4;
+  static constexpr int kBytes = kBar + 256;
+};
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, p_full, dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint32_t tmem_base;
+  int abort_word;
+};
+
+struct BwdParams {
+  const int32_t* tiles;  // fused work list [ntiles][8]; walked backwards
+  long long ntiles;
+  int hq, hkv, group;
+  long long T;
+  float scale, scale_log2;
+  const float* lse;      // [hq][T] natural log
+  const float* dl;       // [hq][T] rowsum(dO * O)
+  float* dq_acc;         // [T][hq][D] fp32, zeroed
+  __nv_bfloat16* dk;     // [T][hkv][D]
+  __nv_bfloat16* dv;
+  unsigned int* err;
+};
+
+struct BwdUnit {
+  int k_row0, k_rows, doc_start, doc_len, j, n, kvh, iters;
+};
+
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, long long u) {
+  const long long ti = u / p.hkv;
+  const int4* row = reinterpret_cast<const int4*>(p.tiles + (p.ntiles - 1 - ti) * 8);
+  const int4 a = __ldg(row), b = __ldg(row + 1);
+  BwdUnit x;
+  x.k_row0 = a.x;
+  x.k_rows = a.y;
+  x.doc_start = a.z;
+  x.doc_len = b.w;
+  x.j = b.y / kTile;
+  x.n = (x.doc_len + kTile - 1) / kTile;
+  x.kvh = static_cast<int>(u - ti * p.hkv);
+  x.iters = p.group * (x.n - x.j);
+  return x;
+}
+
+// Iteration k of a unit: query head and query tile.
+__device__ __forceinline__ void bwd_iter(const BwdParams& p, const BwdUnit& x, int k, int* h, int* i) {
+  const int per = x.n - x.j;
+  *h = x.kvh * p.group + k / per;
+  *i = x.j + k % per;
+}
+
+__device__ __forceinline__ long long bwd_unit_index(long long k, int cta, int nctas) {
+  return k * nctas + ((k & 1) ? (nctas - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ void bwd_drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > kWaitBudgetClocks / 4) break;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    k_attn_bwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + L::kBar);
+  volatile int* abort_word = &bars.abort_word;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total_units = p.ntiles * p.hkv;
+  const int cta = blockIdx.x, nctas = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_empty, 4);
+    mbar_init(&bars.dkv_full, 1);
+    mbar_init(&bars.dkv_empty, 4);
+    mbar_init(&bars.drain, 1);
+    bars.abort_word = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kBwdMma) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kBwdProducer && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const uint32_t tDV = tmem, tDK = tmem + D, tS = tmem + 2 * D, tDP = tmem + 2 * D + 128;
+
+  if (warp == kBwdProducer) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t q_uses[2] = {0, 0};
+      long long it_global = 0;
+      uint32_t units = 0;
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long u = bwd_unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const BwdUnit x = bwd_unit(p, u);
+        if (units > 0 && !mbar_wait(&bars.kv_empty, (units - 1) & 1, abort_word, p.err, kErrBKvE)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars.kv_full, 2 * L::kTileBytes);
+#pragma unroll
+        for (int hb = 0; hb < D / 64; ++hb) {
+          tma_load_3d(smem + L::kK + hb * L::kHalfBytes, &tmK, &bars.kv_full, hb * 64, x.kvh, x.k_row0);
+          tma_load_3d(smem + L::kV + hb * L::kHalfBytes, &tmV, &bars.kv_full, hb * 64, x.kvh, x.k_row0);
+        }
+        ++units;
+        for (int it = 0; it < x.iters; ++it) {
+          int h, i;
+          bwd_iter(p, x, it, &h, &i);
+          const int st = static_cast<int>(it_global & 1);
+          if (q_uses[st] > 0 && !mbar_wait(&bars.q_empty[st], (q_uses[st] - 1) & 1, abort_word, p.err, kErrBQE)) {
+            ok = false;
+            break;
+          }
+          ++q_uses[st];
+          const int q_row0 = x.doc_start + i * kTile;
+          mbar_arrive_expect_tx(&bars.q_full[st], 2 * L::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_load_3d(smem + L::kQ + st * L::kTileBytes + hb * L::kHalfBytes, &tmQ, &bars.q_full[st], hb * 64, h,
+                        q_row0);
+            tma_load_3d(smem + L::kDO + st * L::kTileBytes + hb * L::kHalfBytes, &tmDO, &bars.q_full[st], hb * 64,
+                        h, q_row0);
+          }
+          ++it_global;
+        }
+      }
+      if (!ok) {
+        // every armed barrier completes once its bytes land
+        if (units > 0) bwd_drain_wait(&bars.kv_full, (units - 1) & 1);
+        for (int s = 0; s < 2; ++s)
+          if (q_uses[s] > 0) bwd_drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
+      }
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kBwdThreads);
+  } else if (warp == kBwdMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);   // K-major A and B
+      constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 1);    // A from TMEM, B MN-major
+      constexpr uint32_t idesc_q = idesc_bf16_f32_ab(128, D, 1, 1);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
+      const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + L::kQ), L::kHalfBytes, 1024);
+      const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + L::kDO), L::kHalfBytes, 1024);
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), L::kHalfBytes, 1024);
+      const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + L::kDS), 16384, 1024);
+      long long it_global = 0;
+      uint32_t units = 0;
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long u = bwd_unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const BwdUnit x = bwd_unit(p, u);
+        ok = mbar_wait(&bars.kv_full, units & 1, abort_word, p.err, kErrBKv);
+        if (!ok) break;
+        for (int it = 0; it < x.iters && ok; ++it) {
+          const int st = static_cast<int>(it_global & 1);
+          ok = mbar_wait(&bars.q_full[st], (it_global >> 1) & 1, abort_word, p.err, kErrBQ);
+          if (!ok) break;
+          const uint64_t qk = dQ_k + st * kTileUnits, dok = dDO_k + st * kTileUnits;
+          // S^T = K_j Q_i^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+            umma_ss(tS, dK_k + off, qk + off, idesc_s, kk > 0);
+          }
+          // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
+          if (it_global > 0) {
+            ok = mbar_wait(&bars.dq_empty, (it_global - 1) & 1, abort_word, p.err, kErrBDqE);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+            umma_ss(tDP, dV_k + off, dok + off, idesc_s, kk > 0);
+          }
+          umma_commit(&bars.s_full);
+          // P^T, dS^T in TMEM and dS in smem from the dS warps
+          ok = mbar_wait(&bars.p_full, it_global & 1, abort_word, p.err, kErrBP);
+          if (ok && it == 0 && units > 0)
+            ok = mbar_wait(&bars.dkv_empty, (units - 1) & 1, abort_word, p.err, kErrBDkvE);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t first = it == 0 ? 0u : 1u;
+          const uint64_t qmn = dQ_mn + st * kTileUnits, domn = dDO_mn + st * kTileUnits;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
+            umma_ts(tDV, tS + kk * 8, domn + off, idesc_kv, kk > 0 ? 1u : first);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
+            umma_ts(tDK, tDP + kk * 8, qmn + off, idesc_kv, kk > 0 ? 1u : first);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
+            umma_ss(tDP, dDS_mn + off, dK_mn + off, idesc_q, kk > 0);
+          }
+          umma_commit(&bars.dq_full);
+          umma_commit(&bars.q_empty[st]);
+          if (it == x.iters - 1) {
+            umma_commit(&bars.kv_empty);
+            umma_commit(&bars.dkv_full);
+          }
+          ++it_global;
+        }
+        ++units;
+      }
+      umma_commit(&bars.drain);
+      bwd_drain_wait(&bars.drain, 0);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kBwdThreads);
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ dS warps (thread = key row)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float* lse2_s = reinterpret_cast<float*>(smem + L::kLse);
+    float* dl_s = reinterpret_cast<float*>(smem + L::kDl);
+    uint8_t* ds_row = smem + L::kDS + r * 128;
+    long long it_global = 0;
+    bool ok = true;
+    for (long long k = 0; ok; ++k) {
+      const long long u = bwd_unit_index(k, cta, nctas);
+      if (u >= total_units) break;
+      const BwdUnit x = bwd_unit(p, u);
+      const int key_local = x.j * kTile + r;
+      for (int it = 0; it < x.iters; ++it) {
+        int h, i;
+        bwd_iter(p, x, it, &h, &i);
+        // the previous tile's readers of lse2_s / dl_s are done (and every
+        // warp agrees to go on)
+        if (named_barrier_or(kDsBarrier, 128, !ok)) {
+          ok = false;
+          break;
+        }
+        {
+          const int q_local = i * kTile + r;
+          const bool qv = q_local < x.doc_len;
+          const long long tok = static_cast<long long>(x.doc_start) + q_local;
+          lse2_s[r] = qv ? __ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
+          dl_s[r] = qv ? __ldg(p.dl + static_cast<long long>(h) * p.T + tok) : 0.f;
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, it_global & 1, abort_word, p.err, kErrBS));
+        if (named_barrier_or(kDsBarrier, 128, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int q_base = i * kTile;  // doc-local position of query column 0
+        const bool key_ok = key_local < x.doc_len;
+        // query column c is allowed iff key_local <= q_base + c < doc_len
+        const int c_lo = key_local - q_base;          // first allowed column
+        const int c_hi = x.doc_len - q_base;          // one past the last
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], dpv[32];
+          tmem_ld32(tS + lane_off + c * 32, sv);
+          tmem_ld32(tDP + lane_off + c * 32, dpv);
+          tmem_wait_ld();
+          uint32_t pk_p[16], pk_ds[16];
+          const float4* l4 = reinterpret_cast<const float4*>(lse2_s + c * 32);
+          const float4* d4 = reinterpret_cast<const float4*>(dl_s + c * 32);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 lv = l4[e4], dv = d4[e4];
+            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+            float pp[4], dd[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int e = e4 * 4 + t;
+              const int col = c * 32 + e;
+              const bool allowed = key_ok && col >= c_lo && col < c_hi;
+              const float pe = allowed ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -la[t])) : 0.f;
+              pp[t] = pe;
+              dd[t] = pe * (__uint_as_float(dpv[e]) - da[t]) * p.scale;
+            }
+            pk_p[e4 * 2] = pack_bf16x2(pp[0], pp[1]);
+            pk_p[e4 * 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+            pk_ds[e4 * 2] = pack_bf16x2(dd[0], dd[1]);
+            pk_ds[e4 * 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+          }
+          // P^T / dS^T back into the columns already read (chunk c covers
+          // packed columns [16c, 16c + 16) of S^T and dP^T)
+          tmem_st16(tS + lane_off + c * 16, pk_p);
+          tmem_st16(tDP + lane_off + c * 16, pk_ds);
+          // dS row (this key, 32 queries) into the MN-major tile: query
+          // columns of 8 per 16-byte chunk, 64 per 128-byte row of a half
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cq = c * 4 + q4;
+            uint8_t* dst = ds_row + (cq >> 3) * 16384 + (((cq & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) =
+                make_uint4(pk_ds[q4 * 4], pk_ds[q4 * 4 + 1], pk_ds[q4 * 4 + 2], pk_ds[q4 * 4 + 3]);
+          }
+        }
+        tmem_wait_st();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full);
+        ++it_global;
+      }
+    }
+    named_barrier_sync(1, kBwdThreads);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ warps (thread = query row), dK/dV epilogue
+    const int qq = warp - 4;
+    const int r = qq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qq * 32) << 16;
+    long long it_global = 0;
+    uint32_t units = 0;
+    bool ok = true;
+    for (long long k = 0; ok; ++k) {
+      const long long u = bwd_unit_index(k, cta, nctas);
+      if (u >= total_units) break;
+      const BwdUnit x = bwd_unit(p, u);
+      for (int it = 0; it < x.iters && ok; ++it) {
+        int h, i;
+        bwd_iter(p, x, it, &h, &i);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, it_global & 1, abort_word, p.err, kErrBDq));
+        if (!ok) break;
+        tc_fence_after();
+        const bool row_ok = i * kTile + r < x.doc_len;
+        float* dst = p.dq_acc + ((static_cast<long long>(x.doc_start) + i * kTile + r) * p.hq + h) *
+                                    static_cast<long long>(D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tDP + lane_off + c * 32, v);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              red_add_v4(dst + c * 32 + m * 4, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                         __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dq_empty);
+        ++it_global;
+      }
+      if (!ok) break;
+      // ---- the unit's dK and dV rows (thread = key row)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkv_full, units & 1, abort_word, p.err, kErrBDkv));
+      if (!ok) break;
+      tc_fence_after();
+      const bool key_ok = r < x.k_rows;
+      const long long krow = (static_cast<long long>(x.k_row0) + r) * p.hkv + x.kvh;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + krow * D;
+        const uint32_t col0 = which == 0 ? tDV : tDK;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(col0 + lane_off + c * 32, v);
+          tmem_wait_ld();
+          if (key_ok) {
+            uint4 w[4];
+            uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) wp[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            uint4* d4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d4[e] = w[e];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dkv_empty);
+      ++units;
+    }
+    named_barrier_sync(1, kBwdThreads);
+  } else {
+    named_barrier_sync(1, kBwdThreads);  // idle warps
+  }
+}
+
+// D[h][t] = sum_c dO[t][h][c] * O[t][h][c]; 16 threads per (t, h) row, 8
+// elements (16 bytes) per thread per step.
+template <int D>
+__global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                            float* __restrict__ dl, long long rows, int hq, long long T) {
+  const long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 16;
+  const int sub = threadIdx.x & 15;
+  float acc = 0.f;
+  if (row < rows) {
+#pragma unroll
+    for (int c = sub * 8; c < D; c += 128) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D + c));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * D + c));
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a2[e]), fb = __bfloat1622float2(b2[e]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
+    const long long t = row / hq;
+    const int h = static_cast<int>(row - t * hq);
+    dl[static_cast<long long>(h) * T + t] = acc;
+  }
+}
+
+// fp32 dQ workspace -> bf16 dq (8 elements per thread).
+__global__ void k_bwd_dq_convert(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    uint4 w;
+    w.x = pack_bf16x2(a.x, a.y);
+    w.y = pack_bf16x2(a.z, a.w);
+    w.z = pack_bf16x2(b.x, b.y);
+    w.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+size_t bwd_align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void bwd_workspace(const hdp_plan_s* plan, int hq, int d, size_t* acc_bytes, size_t* total) {
+  const size_t T = static_cast<size_t>(plan->v.total_tokens);
+  *acc_bytes = bwd_align256(T * hq * d * sizeof(float));
+  *total = *acc_bytes + bwd_align256(T * hq * sizeof(float));
+}
+
+template <int D>
+hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, int hq, int hkv, float scale, float* dq_acc, float* dl,
+                        void* dq, void* dk, void* dv, cudaStream_t st) {
+  const long long T = plan->v.total_tokens;
+  if (T == 0) return HDP_OK;
+  CUtensorMap mq, mk, mv, mdo;
+  hdp_status_t r;
+  if ((r = make_bf16_tile_map(&mq, q, T, hq, D)) != HDP_OK) return r;
+  if ((r = make_bf16_tile_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
+  if ((r = make_bf16_tile_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
+  if ((r = make_bf16_tile_map(&mdo, dout, T, hq, D)) != HDP_OK) return r;
+  int dev = 0, sms = 0;
+  HDP_CUDA_TRY(cudaGetDevice(&dev));
+  HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  // D = rowsum(dO * O) and a zeroed dQ accumulator
+  const long long rows = T * hq;
+  k_bwd_delta<D><<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dl, rows, hq, T);
+  note_launch();
+  HDP_CUDA_TRY(cudaGetLastError());
+  HDP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), st));
+  BwdParams prm{};
+  prm.tiles = plan->v.tiles_fused;
+  prm.ntiles = plan->v.num_tiles_fused;
+  prm.hq = hq;
+  prm.hkv = hkv;
+  prm.group = hq / hkv;
+  prm.T = T;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.lse = lse;
+  prm.dl = dl;
+  prm.dq_acc = dq_acc;
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.err = device_error_word();
+  if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
+  const long long units = prm.ntiles * hkv;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  const int smem = BwdSmem<D>::kBytes + 1024;
+  HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);
+  note_launch();
+  HDP_CUDA_TRY(cudaGetLastError());
+  const long long n8 = rows * D / 8;
+  const int cgrid = static_cast<int>(n8 / 256 + 1 < 8L * sms ? n8 / 256 + 1 : 8L * sms);
+  k_bwd_dq_convert<<<cgrid, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+  note_launch();
+  HDP_CUDA_TRY(cudaGetLastError());
+  return HDP_OK;
+}
+
+}  // namespace
+}  // namespace hdp
+
+using namespace hdp;
+
+extern "C" hdp_status_t hdp_attention_bwd_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t d, size_t* bytes) {
+  if (!plan || !bytes) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd_workspace_bytes: NULL argument");
+  if (hq < 1 || d < 1)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd_workspace_bytes: hq, d must be >= 1");
+  size_t acc = 0;
+  bwd_workspace(plan, hq, d, &acc, bytes);
+  return HDP_OK;
+}
+
+extern "C" hdp_status_t hdp_attention_bwd(hdp_plan_t plan, const void* q, const void* k, const void* v,
+                                          const void* o, const float* lse, const void* dout, int32_t hq,
+                                          int32_t hkv, int32_t d, float scale, void* workspace,
+                                          size_t workspace_bytes, void* dq, void* dk, void* dv, void* stream) {
+  if (!plan || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: NULL argument");
+  if (hq < 1 || hkv < 1 || hq % hkv != 0)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: need hq >= 1, hkv >= 1, hq % hkv == 0");
+  if (!(scale > 0.f)) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: scale must be > 0");
+  if (d != 64 && d != 128) return fail(HDP_ERR_UNSUPPORTED, "hdp_attention_bwd: d must be 64 or 128");
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  if (mis & 15)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: q, k, v, o, dout, dq, dk, dv must be 16-byte aligned");
+  size_t acc = 0, need = 0;
+  bwd_workspace(plan, hq, d, &acc, &need);
+  if (!workspace || workspace_bytes < need)
+    return fail(HDP_ERR_INVALID_ARGUMENT,
+                "hdp_attention_bwd: workspace too small (need " + std::to_string(need) + " bytes)");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: workspace must be 256-byte aligned");
+  float* dq_acc = static_cast<float*>(workspace);
+  float* dl = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dq_acc, dl, dq, dk, dv, st)
+                  : launch_bwd<64>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dq_acc, dl, dq, dk, dv, st);
+}

@@ -614,6 +614,15 @@ hdp_status_t make_map(CUtensorMap* m, const void* base, long long T, int heads, 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+}  // namespace
+
+// Shared with the backward pass: the same tile map for any [T][heads][d] bf16 tensor.
+hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, int heads, int d) {
+  return make_map(m, base, T, heads, d);
+}
+
+namespace {
+
 template <int D>
 hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const void* v, int hq, int hkv,
                     float scale, bool split, float* o_part, float* lse_part, void* o, float* lse, cudaStream_t st) {

@@ -346,10 +346,10 @@ __device__ __forceinline__ unsigned long long tile_key(long long weight, long lo
 }
 
 __device__ __forceinline__ void store_tile(int32_t* out, long long t, int32_t q0, int32_t qrows, int32_t kv0,
-                                           int32_t kvlen, int32_t blk, int32_t row_off, int32_t w) {
+                                           int32_t kvlen, int32_t blk, int32_t row_off, int32_t w, int32_t doc_len) {
   int4* o = reinterpret_cast<int4*>(out + t * 8);
   o[0] = make_int4(q0, qrows, kv0, kvlen);
-  o[1] = make_int4(blk, row_off, w, 0);
+  o[1] = make_int4(blk, row_off, w, doc_len);
 }
 
 // One row per document query tile: keys are the document's causal prefix.
@@ -365,7 +365,8 @@ __global__ void k_fill_tiles_fused(int32_t n, long long ntiles, const int32_t* _
     const long long kvlen = qt * kTile + qrows;
     const long long w = qt + 1;
     store_tile(rows, t, static_cast<int32_t>(cu[doc] + qt * kTile), static_cast<int32_t>(qrows), cu[doc],
-               static_cast<int32_t>(kvlen), -1, static_cast<int32_t>(qt * kTile), static_cast<int32_t>(w));
+               static_cast<int32_t>(kvlen), -1, static_cast<int32_t>(qt * kTile), static_cast<int32_t>(w),
+               static_cast<int32_t>(s));
     keys[t] = tile_key(w, t);
   }
 }
@@ -405,7 +406,7 @@ __global__ void k_fill_tiles_split(int32_t n, int32_t C, long long ntiles, const
     store_tile(rows, t, static_cast<int32_t>(cu[doc] + qc * C + qt * kTile), static_cast<int32_t>(qrows),
                static_cast<int32_t>(cu[doc] + kc * C), static_cast<int32_t>(kvlen),
                static_cast<int32_t>(bo[doc] + blk_local), static_cast<int32_t>(qt * kTile),
-               static_cast<int32_t>(w));
+               static_cast<int32_t>(w), 0);
     keys[t] = tile_key(w, t);
   }
 }

@@ -117,3 +117,8 @@ def test_document_independence_and_dq_rows():
     heads = np.array([0, 3, 1, 2, 0], np.int32)
     rows = oracle.attention_bwd_dq_rows(*packed, cu, hq, hkv, d, 0.35, toks, heads)
     assert np.array_equal(rows, dq[toks, heads])
+    kt = np.array([0, 5, 6, 16, 17, 19])
+    kh = np.zeros(len(kt), np.int32)
+    dk_r, dv_r = oracle.attention_bwd_dkv_rows(*packed, cu, hq, hkv, d, 0.35, kt, kh)
+    assert np.allclose(dk_r, dk[kt, 0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(dv_r, dv[kt, 0], rtol=1e-12, atol=1e-14)

@@ -313,8 +313,14 @@ def test_tile_worklist_covers_every_causal_pair_once(split):
     T = sum(lengths)
     doc = np.repeat(np.arange(len(lengths)), lengths)
     cover = np.zeros((T, T), np.int32)
-    for q0, qrows, kv0, kvlen, blk, off, w, _ in wlst:
+    starts = np.concatenate([[0], np.cumsum(lengths)])
+    for q0, qrows, kv0, kvlen, blk, off, w, slen in wlst:
         assert w == -(-kvlen // tile)
+        # the last column is the query's document length (fused list only)
+        d_i = doc[q0]
+        assert slen == (0 if split else lengths[d_i])
+        if not split:
+            assert kv0 == starts[d_i] and off == q0 - starts[d_i]
         for t in range(q0, q0 + qrows):
             for u in range(kv0, kv0 + kvlen):
                 if u <= t:
