@@ -602,6 +602,62 @@ def balance_mode(args):
     return 0
 
 
+def backward_mode(args):
+    """Backward pass (dq, dk, dv) after the forward of the same micro-batch,
+    on --workload.  CUDA events around each call; the backward's useful FLOPs
+    are 2.5 x the forward's (five products of the forward's shape instead of
+    two: S, dP, dV, dK, dQ).  One JSON line."""
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import build as native_build
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = wl.workload(args.workload, args.seed)
+    q, k, v = wl.qkv(w, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(args.seed + 1)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    T = w.total_tokens
+    lengths_d = torch.tensor(w.lengths, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    plan = pkg.hdp_plan_create(lengths_d, w.capacity)
+    ws = torch.empty(pkg.hdp_attention_bwd_workspace_bytes(plan, w.hq, w.d), dtype=torch.uint8, device=dev)
+    flops_fwd = useful_flops(w.lengths, w.d, w.hq)
+    flops_bwd = flops_fwd * 5 // 2
+    peaks, src = load_peaks()
+    fwd_ms, bwd_ms = [], []
+    with ClockSampler(0) as clocks:
+        for it in range(args.warmup + args.steps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, pkg.HDP_MODE_FUSED, None, o, lse)
+            e[1].record()
+            pkg.hdp_attention_bwd(plan, q, k, v, o, lse, dout, w.hq, w.hkv, w.d, w.scale, ws, dq, dk, dv)
+            e[2].record()
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                fwd_ms.append(e[0].elapsed_time(e[1]))
+                bwd_ms.append(e[1].elapsed_time(e[2]))
+    pkg.hdp_device_status()
+    plan.destroy()
+    fm, bm = statistics.median(fwd_ms), statistics.median(bwd_ms)
+    bw = flops_bwd / (bm * 1e-3) / 1e12
+    out = {"mode": "backward", "workload": workload_config(w, args, "fused")["workload"], "steps": args.steps, "warmup": args.warmup,
+           "fwd_ms": fm, "bwd_ms": bm, "fwd_tflops": flops_fwd / (fm * 1e-3) / 1e12, "bwd_tflops": bw,
+           "step_tflops": (flops_fwd + flops_bwd) / ((fm + bm) * 1e-3) / 1e12,
+           "roofline": {"bound": "tensor", "kernel": "k_attn_bwd (+ delta and dq conversion)", "achieved": bw,
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": bw / peaks["bf16_tflops"],
+                        "peak_source": src},
+           "clocks": clocks.summary()}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,6 +674,8 @@ def main():
                     help="calibrate T(s) and t_blk on this GPU and apply the ring model")
     ap.add_argument("--balance", action="store_true",
                     help="balance scheduler on the per-shard FLOPs of the 1M-token mixture")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (after the forward) on --workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -628,6 +686,8 @@ def main():
         return cost_model_mode(args) if rank == 0 else 0
     if args.balance:
         return balance_mode(args) if rank == 0 else 0
+    if args.backward:
+        return backward_mode(args) if rank == 0 else 0
     if args.impl == "reference":
         return reference_arm(args, rank)
     return our_arm(args, ws, rank, local)

@@ -14,18 +14,24 @@
 // key tile's diagonal on, so fully masked tiles are never touched.  dK and dV
 // of the unit accumulate in TMEM for the whole unit; dQ of each query tile is
 // produced in TMEM and added into an fp32 workspace.
-//   warps 0-3  dS warps: thread = key row.  S^T and dP^T (keys on the TMEM
-//              lanes) -> P^T and dS^T in bf16, written back into TMEM for the
-//              dV / dK MMAs and dS into shared memory for the dQ MMA
-//   warps 4-7  dQ warps: thread = query row of the dQ tile -> vector atomic
-//              adds; at the end of a unit, dK and dV rows -> bf16 outputs
+//   warps 0-7  compute warps (two per scheduler: TMEM lane quarter w % 4,
+//              column half w / 4), in turn for each query tile:
+//              dS  thread = key row.  S^T and dP^T (keys on the TMEM lanes)
+//                  -> P^T and dS^T in bf16, written back into TMEM for the
+//                  dV / dK MMAs, and dS into shared memory for the dQ MMA;
+//              dQ  thread = query row.  The dQ tile is read into registers
+//                  (freeing TMEM for the next tile at once), staged in shared
+//                  memory and added into the fp32 accumulator by TMA
+//                  reduce-adds (full lines);
+//              and at the end of a unit the dK and dV rows -> bf16 outputs
 //   warp 8     TMA producer        warp 9     MMA issuer + TMEM owner
 // Per query tile i of the unit (key tile j):
 //   S^T  = K_j Q_i^T      dP^T = V_j dO_i^T           (SS, M = keys)
 //   dV  += P^T dO_i       dK  += dS^T Q_i             (TS, A from TMEM)
 //   dQ_i  = dS K_j                                    (SS, A = dS in smem, MN-major)
 // TMEM (512 columns): dV [0,D) dK [D,2D) S^T [2D,2D+128) dP^T [2D+128,2D+256);
-// P^T aliases S^T's first 64 columns, dS^T and then dQ alias dP^T's.
+// P^T aliases S^T's columns [0,32) and [64,96) (one block per column half),
+// dS^T the same columns of dP^T, and then dQ aliases dP^T.
 // Every wait is bounded; a timeout sets the device error word and all roles
 // stop at the same point, drain and free TMEM.
 #include <cuda.h>
@@ -40,13 +46,14 @@
 namespace hdp {
 
 hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, int heads, int d);
+hdp_status_t make_f32_reduce_map(CUtensorMap* m, void* base, long long T, int heads, int d);
 
 namespace {
 
 constexpr int kBwdThreads = 384;
 constexpr int kBwdProducer = 8;
 constexpr int kBwdMma = 9;
-constexpr uint32_t kDsBarrier = 2;  // named barrier of the four dS warps
+constexpr uint32_t kDsBarrier = 2;  // named barrier of the eight compute warps
 
 constexpr int kErrBKv = 0x201, kErrBQ = 0x202, kErrBS = 0x203, kErrBP = 0x204, kErrBDq = 0x205,
               kErrBDqE = 0x206, kErrBDkv = 0x207, kErrBDkvE = 0x208, kErrBKvE = 0x209, kErrBQE = 0x20a;
@@ -108,11 +115,15 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, long long u) {
   return x;
 }
 
-// Iteration k of a unit: query head and query tile.
+// Iteration k of a unit: query head and query tile.  Query tiles run from
+// the document's last tile down to the key tile's diagonal, so every unit of
+// a document starts at the same tile: the CTAs working on one GQA group read
+// the same Q / dO tiles and add into the same dQ rows at about the same time,
+// and those stay in L2.
 __device__ __forceinline__ void bwd_iter(const BwdParams& p, const BwdUnit& x, int k, int* h, int* i) {
   const int per = x.n - x.j;
   *h = x.kvh * p.group + k / per;
-  *i = x.j + k % per;
+  *i = x.n - 1 - k % per;
 }
 
 __device__ __forceinline__ long long bwd_unit_index(long long k, int cta, int nctas) {
@@ -131,7 +142,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_attn_bwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -149,11 +160,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars.q_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.p_full, 8);
     mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_empty, 4);
+    mbar_init(&bars.dq_empty, 8);
     mbar_init(&bars.dkv_full, 1);
-    mbar_init(&bars.dkv_empty, 4);
+    mbar_init(&bars.dkv_empty, 8);
     mbar_init(&bars.drain, 1);
     bars.abort_word = 0;
     fence_mbarrier_init();
@@ -167,6 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -285,12 +297,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
-            umma_ts(tDV, tS + kk * 8, domn + off, idesc_kv, kk > 0 ? 1u : first);
+            umma_ts(tDV, tS + kk * 8 + (kk >= 4 ? 32 : 0), domn + off, idesc_kv, kk > 0 ? 1u : first);
           }
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
-            umma_ts(tDK, tDP + kk * 8, qmn + off, idesc_kv, kk > 0 ? 1u : first);
+            umma_ts(tDK, tDP + kk * 8 + (kk >= 4 ? 32 : 0), qmn + off, idesc_kv, kk > 0 ? 1u : first);
           }
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -315,14 +327,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     named_barrier_sync(1, kBwdThreads);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ dS warps (thread = key row)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warps 0-7
+    // Warp w serves TMEM lane quarter qt = w % 4 (32 rows) and column half
+    // hf = w / 4, so two warps share each scheduler and split every phase:
+    //   dS   (thread = key row): S^T / dP^T columns [64 hf, 64 hf + 64)
+    //   dQ   (thread = query row): dQ columns [hf D/2, hf D/2 + D/2)
+    //   end of unit (thread = key row): dK / dV columns [hf D/2, hf D/2 + D/2)
+    const int qt = warp & 3, hf = warp >> 2;
+    const int r = qt * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qt * 32) << 16;
     float* lse2_s = reinterpret_cast<float*>(smem + L::kLse);
     float* dl_s = reinterpret_cast<float*>(smem + L::kDl);
-    uint8_t* ds_row = smem + L::kDS + r * 128;
+    uint8_t* ds_row = smem + L::kDS + hf * 16384 + r * 128;
+    // dQ staging: this warp's 4 KB of the dS tile's smem (one 32-row x
+    // 32-column fp32 box, 128-byte swizzled as the reduce map expects)
+    uint8_t* stage = smem + L::kDS + warp * 4096;
     long long it_global = 0;
+    uint32_t units = 0;
     bool ok = true;
     for (long long k = 0; ok; ++k) {
       const long long u = bwd_unit_index(k, cta, nctas);
@@ -332,32 +354,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int it = 0; it < x.iters; ++it) {
         int h, i;
         bwd_iter(p, x, it, &h, &i);
-        // the previous tile's readers of lse2_s / dl_s are done (and every
-        // warp agrees to go on)
-        if (named_barrier_or(kDsBarrier, 128, !ok)) {
+        // every compute warp is done with the previous tile (its LSE / D
+        // reads and its dQ staging reads), and all agree to go on
+        if (named_barrier_or(kDsBarrier, 256, !ok)) {
           ok = false;
           break;
         }
         {
-          const int q_local = i * kTile + r;
+          const int t = threadIdx.x & 127;
+          const int q_local = i * kTile + t;
           const bool qv = q_local < x.doc_len;
           const long long tok = static_cast<long long>(x.doc_start) + q_local;
-          lse2_s[r] = qv ? __ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
-          dl_s[r] = qv ? __ldg(p.dl + static_cast<long long>(h) * p.T + tok) : 0.f;
+          if (threadIdx.x < 128)
+            lse2_s[t] = qv ? __ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
+          else
+            dl_s[t] = qv ? __ldg(p.dl + static_cast<long long>(h) * p.T + tok) : 0.f;
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, it_global & 1, abort_word, p.err, kErrBS));
-        if (named_barrier_or(kDsBarrier, 128, !ok)) {
+        if (named_barrier_or(kDsBarrier, 256, !ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int q_base = i * kTile;  // doc-local position of query column 0
+        // ---- dS: P^T = exp2(S^T scale log2e - lse2), dS^T = P^T (dP^T - D) scale
+        const int q_base = i * kTile;
         const bool key_ok = key_local < x.doc_len;
-        // query column c is allowed iff key_local <= q_base + c < doc_len
-        const int c_lo = key_local - q_base;          // first allowed column
-        const int c_hi = x.doc_len - q_base;          // one past the last
+        const int c_lo = key_local - q_base;  // query column c allowed iff c_lo <= c < c_hi
+        const int c_hi = x.doc_len - q_base;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = hf * 2 + cc;  // 32-column chunk of S^T / dP^T
           uint32_t sv[32], dpv[32];
           tmem_ld32(tS + lane_off + c * 32, sv);
           tmem_ld32(tDP + lane_off + c * 32, dpv);
@@ -384,84 +410,87 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk_ds[e4 * 2] = pack_bf16x2(dd[0], dd[1]);
             pk_ds[e4 * 2 + 1] = pack_bf16x2(dd[2], dd[3]);
           }
-          // P^T / dS^T back into the columns already read (chunk c covers
-          // packed columns [16c, 16c + 16) of S^T and dP^T)
-          tmem_st16(tS + lane_off + c * 16, pk_p);
-          tmem_st16(tDP + lane_off + c * 16, pk_ds);
-          // dS row (this key, 32 queries) into the MN-major tile: query
-          // columns of 8 per 16-byte chunk, 64 per 128-byte row of a half
+          // P^T / dS^T (bf16 pairs) into this half's own columns, already
+          // read: half hf owns S^T / dP^T columns [64 hf, 64 hf + 64), and
+          // chunk c's pairs go to [64 hf + 16 cc, 64 hf + 16 cc + 16)
+          tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk_p);
+          tmem_st16(tDP + lane_off + hf * 64 + cc * 16, pk_ds);
+          // dS row (this key, 32 queries) into the MN-major tile of half hf
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const int cq = c * 4 + q4;
-            uint8_t* dst = ds_row + (cq >> 3) * 16384 + (((cq & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) =
+            const int cq = cc * 4 + q4;  // 16-byte chunk within the 128-byte row
+            *reinterpret_cast<uint4*>(ds_row + ((cq ^ (r & 7)) << 4)) =
                 make_uint4(pk_ds[q4 * 4], pk_ds[q4 * 4 + 1], pk_ds[q4 * 4 + 2], pk_ds[q4 * 4 + 3]);
           }
         }
         tmem_wait_st();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
-        ++it_global;
-      }
-    }
-    named_barrier_sync(1, kBwdThreads);
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dQ warps (thread = query row), dK/dV epilogue
-    const int qq = warp - 4;
-    const int r = qq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(qq * 32) << 16;
-    long long it_global = 0;
-    uint32_t units = 0;
-    bool ok = true;
-    for (long long k = 0; ok; ++k) {
-      const long long u = bwd_unit_index(k, cta, nctas);
-      if (u >= total_units) break;
-      const BwdUnit x = bwd_unit(p, u);
-      for (int it = 0; it < x.iters && ok; ++it) {
-        int h, i;
-        bwd_iter(p, x, it, &h, &i);
+        // ---- dQ (thread = query row): registers first, then TMEM is free
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, it_global & 1, abort_word, p.err, kErrBDq));
-        if (!ok) break;
-        tc_fence_after();
-        const bool row_ok = i * kTile + r < x.doc_len;
-        float* dst = p.dq_acc + ((static_cast<long long>(x.doc_start) + i * kTile + r) * p.hq + h) *
-                                    static_cast<long long>(D);
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tDP + lane_off + c * 32, v);
-          tmem_wait_ld();
-          if (row_ok) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              red_add_v4(dst + c * 32 + m * 4, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                         __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
-          }
+        if (named_barrier_or(kDsBarrier, 256, !ok)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        uint32_t dqv[D / 2];
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tmem_ld32(tDP + lane_off + hf * (D / 2) + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dqv + c * 32));
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.dq_empty);
+        // rows past the document end are staged as zeros (adding nothing)
+        const bool row_ok = i * kTile + r < x.doc_len;
+        const int box_row = x.doc_start + i * kTile + qt * 32;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          if (c > 0) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
+          uint8_t* row = stage + lane * 128;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 w = row_ok ? make_uint4(dqv[c * 32 + 4 * e], dqv[c * 32 + 4 * e + 1], dqv[c * 32 + 4 * e + 2],
+                                                dqv[c * 32 + 4 * e + 3])
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(row + ((e ^ (lane & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tmDQ, stage, hf * (D / 2) + c * 32, h, box_row);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
         ++it_global;
       }
       if (!ok) break;
       // ---- the unit's dK and dV rows (thread = key row)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkv_full, units & 1, abort_word, p.err, kErrBDkv));
-      if (!ok) break;
+      if (named_barrier_or(kDsBarrier, 256, !ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const bool key_ok = r < x.k_rows;
+      const bool kv_ok = r < x.k_rows;
       const long long krow = (static_cast<long long>(x.k_row0) + r) * p.hkv + x.kvh;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + krow * D;
-        const uint32_t col0 = which == 0 ? tDV : tDK;
+        __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + krow * D + hf * (D / 2);
+        const uint32_t col0 = (which == 0 ? tDV : tDK) + hf * (D / 2);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
           tmem_ld32(col0 + lane_off + c * 32, v);
           tmem_wait_ld();
-          if (key_ok) {
+          if (kv_ok) {
             uint4 w[4];
             uint32_t* wp = reinterpret_cast<uint32_t*>(w);
 #pragma unroll
@@ -477,6 +506,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bars.dkv_empty);
       ++units;
     }
+    if (lane == 0) bulk_wait_group0();  // every dQ reduce has landed
+    __syncwarp();
     named_barrier_sync(1, kBwdThreads);
   } else {
     named_barrier_sync(1, kBwdThreads);  // idle warps
@@ -550,6 +581,8 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   if ((r = make_bf16_tile_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_bf16_tile_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_bf16_tile_map(&mdo, dout, T, hq, D)) != HDP_OK) return r;
+  CUtensorMap mdq;
+  if ((r = make_f32_reduce_map(&mdq, dq_acc, T, hq, D)) != HDP_OK) return r;
   int dev = 0, sms = 0;
   HDP_CUDA_TRY(cudaGetDevice(&dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -580,7 +613,7 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   const int grid = static_cast<int>(units < sms ? units : sms);
   const int smem = BwdSmem<D>::kBytes + 1024;
   HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);
+  k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, mdq, prm);
   note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   const long long n8 = rows * D / 8;
