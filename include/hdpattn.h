@@ -190,7 +190,8 @@ hdp_status_t hdp_attention_fwd_split_noalloc(hdp_plan_t plan, const void* q, con
  *   lse: [hq][T] fp32, natural log, as written by hdp_attention_fwd for this
  *   plan (FUSED or SPLIT) and `o` its output.
  * workspace: device, 256-byte aligned, at least
- * hdp_attention_bwd_workspace_bytes (an fp32 dq accumulator and D).
+ * hdp_attention_bwd_workspace_bytes (D in fp32).  Deterministic: no atomics;
+ * dq, dk and dv each accumulate in one CTA in a fixed order.
  * d == 64 or 128 (UNSUPPORTED otherwise); tensor pointers 16-byte aligned.
  * Every output row is written.
  */

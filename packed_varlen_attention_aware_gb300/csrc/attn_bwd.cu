@@ -8,30 +8,29 @@
 // With P = exp(scale Q K^T - LSE) (causal, same document), D = rowsum(dO * O):
 //   dV = P^T dO,  dS = P * (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Design (one persistent CTA per SM, 12 warps).  A work unit is one key tile
-// (128 keys of one document) for one key/value head; it walks every query
-// head of that head's GQA group and every query tile of the document from the
-// key tile's diagonal on, so fully masked tiles are never touched.  dK and dV
-// of the unit accumulate in TMEM for the whole unit; dQ of each query tile is
-// produced in TMEM and added into an fp32 workspace.
+// Two persistent kernels (one CTA per SM, 12 warps), so that no partial sum
+// ever goes through global memory:
+//  - dK/dV pass: a work unit is one key tile (128 keys of one document) for
+//    one key/value head; it walks every query head of that head's GQA group
+//    and every query tile of the document from the key tile's diagonal on
+//    (fully masked tiles are never touched); dK and dV accumulate in TMEM.
+//  - dQ pass (further below): a unit is one query tile of one query head; it
+//    walks the causal key tiles; dQ accumulates in TMEM.
+// S and dP are computed by both passes (seven tile products instead of
+// five), in exchange for no dQ reductions, which on this GPU are bounded by
+// the L2's reduction throughput.
 //   warps 0-7  compute warps (two per scheduler: TMEM lane quarter w % 4,
-//              column half w / 4), in turn for each query tile:
-//              dS  thread = key row.  S^T and dP^T (keys on the TMEM lanes)
-//                  -> P^T and dS^T in bf16, written back into TMEM for the
-//                  dV / dK MMAs, and dS into shared memory for the dQ MMA;
-//              dQ  thread = query row.  The dQ tile is read into registers
-//                  (freeing TMEM for the next tile at once), staged in shared
-//                  memory and added into the fp32 accumulator by TMA
-//                  reduce-adds (full lines);
-//              and at the end of a unit the dK and dV rows -> bf16 outputs
+//              column half w / 4): thread = key row.  S^T and dP^T (keys on
+//              the TMEM lanes) -> P^T and dS^T in bf16, written back into
+//              TMEM for the dV / dK MMAs; at the end of a unit the dK and dV
+//              rows -> bf16 outputs
 //   warp 8     TMA producer        warp 9     MMA issuer + TMEM owner
-// Per query tile i of the unit (key tile j):
+// dK/dV pass, per query tile i of the unit (key tile j):
 //   S^T  = K_j Q_i^T      dP^T = V_j dO_i^T           (SS, M = keys)
 //   dV  += P^T dO_i       dK  += dS^T Q_i             (TS, A from TMEM)
-//   dQ_i  = dS K_j                                    (SS, A = dS in smem, MN-major)
 // TMEM (512 columns): dV [0,D) dK [D,2D) S^T [2D,2D+128) dP^T [2D+128,2D+256);
 // P^T aliases S^T's columns [0,32) and [64,96) (one block per column half),
-// dS^T the same columns of dP^T, and then dQ aliases dP^T.
+// dS^T the same columns of dP^T.
 // Every wait is bounded; a timeout sets the device error word and all roles
 // stop at the same point, drain and free TMEM.
 #include <cuda.h>
@@ -66,8 +65,7 @@ struct BwdSmem {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;           // 2 stages
   static constexpr int kDO = kQ + 2 * kTileBytes;      // 2 stages
-  static constexpr int kDS = kDO + 2 * kTileBytes;     // 128 keys x 128 queries bf16, MN-major
-  static constexpr int kLse = kDS + kTile * kTile * 2; // 128 fp32: LSE * log2(e) of the tile's queries
+  static constexpr int kLse = kDO + 2 * kTileBytes;    // 128 fp32: LSE * log2(e) of the tile's queries
   static constexpr int kDl = kLse + kTile * 4;         // 128 fp32: D of the tile's queries
   static constexpr int kBar = kDl + kTile * 4;
   static constexpr int kBytes = kBar + 256;
@@ -76,7 +74,7 @@ struct BwdSmem {
 struct BwdBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, p_full, dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint64_t s_full, p_full, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort_word;
 };
@@ -89,7 +87,7 @@ struct BwdParams {
   float scale, scale_log2;
   const float* lse;      // [hq][T] natural log
   const float* dl;       // [hq][T] rowsum(dO * O)
-  float* dq_acc;         // [T][hq][D] fp32, zeroed
+  __nv_bfloat16* dq;     // [T][hq][D]
   __nv_bfloat16* dk;     // [T][hkv][D]
   __nv_bfloat16* dv;
   unsigned int* err;
@@ -142,7 +140,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_attn_bwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+               const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,8 +159,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.p_full, 8);
-    mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_empty, 8);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.dkv_empty, 8);
     mbar_init(&bars.drain, 1);
@@ -178,7 +174,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
-    prefetch_tmap(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -244,7 +239,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);   // K-major A and B
       constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 1);    // A from TMEM, B MN-major
-      constexpr uint32_t idesc_q = idesc_bf16_f32_ab(128, D, 1, 1);
       constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
       const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
@@ -252,8 +246,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
       const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + L::kQ), L::kHalfBytes, 1024);
       const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + L::kDO), L::kHalfBytes, 1024);
-      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), L::kHalfBytes, 1024);
-      const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + L::kDS), 16384, 1024);
       long long it_global = 0;
       uint32_t units = 0;
       bool ok = true;
@@ -274,12 +266,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
             umma_ss(tS, dK_k + off, qk + off, idesc_s, kk > 0);
           }
-          // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
-          if (it_global > 0) {
-            ok = mbar_wait(&bars.dq_empty, (it_global - 1) & 1, abort_word, p.err, kErrBDqE);
-            if (!ok) break;
-            tc_fence_after();
-          }
+          // dP^T = V_j dO_i^T (dS^T of the previous tile, in these columns, was
+          // read by its dK MMA, issued earlier)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
@@ -304,12 +292,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
             umma_ts(tDK, tDP + kk * 8 + (kk >= 4 ? 32 : 0), qmn + off, idesc_kv, kk > 0 ? 1u : first);
           }
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
-            umma_ss(tDP, dDS_mn + off, dK_mn + off, idesc_q, kk > 0);
-          }
-          umma_commit(&bars.dq_full);
           umma_commit(&bars.q_empty[st]);
           if (it == x.iters - 1) {
             umma_commit(&bars.kv_empty);
@@ -339,10 +321,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(qt * 32) << 16;
     float* lse2_s = reinterpret_cast<float*>(smem + L::kLse);
     float* dl_s = reinterpret_cast<float*>(smem + L::kDl);
-    uint8_t* ds_row = smem + L::kDS + hf * 16384 + r * 128;
-    // dQ staging: this warp's 4 KB of the dS tile's smem (one 32-row x
-    // 32-column fp32 box, 128-byte swizzled as the reduce map expects)
-    uint8_t* stage = smem + L::kDS + warp * 4096;
     long long it_global = 0;
     uint32_t units = 0;
     bool ok = true;
@@ -415,60 +393,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // chunk c's pairs go to [64 hf + 16 cc, 64 hf + 16 cc + 16)
           tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk_p);
           tmem_st16(tDP + lane_off + hf * 64 + cc * 16, pk_ds);
-          // dS row (this key, 32 queries) into the MN-major tile of half hf
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int cq = cc * 4 + q4;  // 16-byte chunk within the 128-byte row
-            *reinterpret_cast<uint4*>(ds_row + ((cq ^ (r & 7)) << 4)) =
-                make_uint4(pk_ds[q4 * 4], pk_ds[q4 * 4 + 1], pk_ds[q4 * 4 + 2], pk_ds[q4 * 4 + 3]);
-          }
         }
         tmem_wait_st();
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
-        // ---- dQ (thread = query row): registers first, then TMEM is free
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, it_global & 1, abort_word, p.err, kErrBDq));
-        if (named_barrier_or(kDsBarrier, 256, !ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t dqv[D / 2];
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tmem_ld32(tDP + lane_off + hf * (D / 2) + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dqv + c * 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.dq_empty);
-        // rows past the document end are staged as zeros (adding nothing)
-        const bool row_ok = i * kTile + r < x.doc_len;
-        const int box_row = x.doc_start + i * kTile + qt * 32;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          if (c > 0) {
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-          }
-          uint8_t* row = stage + lane * 128;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 w = row_ok ? make_uint4(dqv[c * 32 + 4 * e], dqv[c * 32 + 4 * e + 1], dqv[c * 32 + 4 * e + 2],
-                                                dqv[c * 32 + 4 * e + 3])
-                                   : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(row + ((e ^ (lane & 7)) << 4)) = w;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(&tmDQ, stage, hf * (D / 2) + c * 32, h, box_row);
-            bulk_commit_group();
-          }
-        }
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
         ++it_global;
       }
       if (!ok) break;
@@ -506,11 +435,322 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bars.dkv_empty);
       ++units;
     }
-    if (lane == 0) bulk_wait_group0();  // every dQ reduce has landed
-    __syncwarp();
     named_barrier_sync(1, kBwdThreads);
   } else {
     named_barrier_sync(1, kBwdThreads);  // idle warps
+  }
+}
+
+// ---------------------------------------------------------------- dQ pass
+// Query-stationary: a unit is one query tile of one query head (the forward's
+// heaviest-first work list, the heads of a tile next to each other so the CTAs
+// of one GQA group read the same K / V tiles).  Per key tile j of the causal
+// range: S = Q K_j^T, dP = dO V_j^T (SS), then dS = P * (dP - D) * scale from the
+// compute warps into S's TMEM columns, and dQ += dS K_j (TS, A from TMEM).  dQ
+// accumulates in TMEM over the whole range and is written once, in bf16.
+// TMEM: S two buffers [0,128) [128,256), dP [256,384), dQ [384,384+D).  While
+// the compute warps work on tile j the MMA thread already computes S(j+1) and,
+// once they have read dP(j), dP(j+1).
+template <int D>
+struct DqSmem {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kHalfBytes = kTile * 64 * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTileBytes;
+  static constexpr int kK = kDO + kTileBytes;      // 2 stages
+  static constexpr int kV = kK + 2 * kTileBytes;   // 2 stages
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kBytes = kBar + 256;
+};
+
+struct DqBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full, dp_free, p_full[2], dq_full, dq_empty, drain;
+  uint32_t tmem_base;
+  int abort_word;
+};
+
+constexpr int kErrDQ = 0x301, kErrDKv = 0x302, kErrDS = 0x303, kErrDDp = 0x304, kErrDP = 0x305, kErrDDq = 0x306,
+              kErrDDqE = 0x307, kErrDQE = 0x308, kErrDKvE = 0x309;
+
+struct DqUnit {
+  int q_row0, q_rows, doc_start, doc_len, i, ntk, h, kvh;
+};
+
+__device__ __forceinline__ DqUnit dq_unit(const BwdParams& p, long long u) {
+  const long long ti = u / p.hq;
+  const int4* row = reinterpret_cast<const int4*>(p.tiles + ti * 8);
+  const int4 a = __ldg(row), b = __ldg(row + 1);
+  DqUnit x;
+  x.q_row0 = a.x;
+  x.q_rows = a.y;
+  x.doc_start = a.z;
+  x.ntk = (a.w + kTile - 1) / kTile;  // key tiles of the causal range
+  x.i = b.y / kTile;
+  x.doc_len = b.w;
+  x.h = static_cast<int>(u - ti * p.hq);
+  x.kvh = x.h / p.group;
+  return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    k_attn_bwd_dq(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  using L = DqSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqBars& bars = *reinterpret_cast<DqBars*>(smem + L::kBar);
+  volatile int* abort_word = &bars.abort_word;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total_units = p.ntiles * p.hq;
+  const int cta = blockIdx.x, nctas = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_free, 8);
+    // two barriers for P: the compute warps could otherwise finish the tile
+    // after next before the MMA thread has seen this one
+    mbar_init(&bars.p_full[0], 8);
+    mbar_init(&bars.p_full[1], 8);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_empty, 8);
+    mbar_init(&bars.drain, 1);
+    bars.abort_word = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kBwdMma) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kBwdProducer && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
+
+  if (warp == kBwdProducer) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t units = 0, kv_uses[2] = {0, 0};
+      long long kvc = 0;
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long u = bwd_unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const DqUnit x = dq_unit(p, u);
+        if (units > 0 && !mbar_wait(&bars.q_empty, (units - 1) & 1, abort_word, p.err, kErrDQE)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars.q_full, 2 * L::kTileBytes);
+#pragma unroll
+        for (int hb = 0; hb < D / 64; ++hb) {
+          tma_load_3d(smem + L::kQ + hb * L::kHalfBytes, &tmQ, &bars.q_full, hb * 64, x.h, x.q_row0);
+          tma_load_3d(smem + L::kDO + hb * L::kHalfBytes, &tmDO, &bars.q_full, hb * 64, x.h, x.q_row0);
+        }
+        ++units;
+        for (int j = 0; j < x.ntk; ++j) {
+          const int st = static_cast<int>(kvc & 1);
+          if (kv_uses[st] > 0 &&
+              !mbar_wait(&bars.kv_empty[st], (kv_uses[st] - 1) & 1, abort_word, p.err, kErrDKvE)) {
+            ok = false;
+            break;
+          }
+          ++kv_uses[st];
+          mbar_arrive_expect_tx(&bars.kv_full[st], 2 * L::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_load_3d(smem + L::kK + st * L::kTileBytes + hb * L::kHalfBytes, &tmK, &bars.kv_full[st], hb * 64,
+                        x.kvh, x.doc_start + j * kTile);
+            tma_load_3d(smem + L::kV + st * L::kTileBytes + hb * L::kHalfBytes, &tmV, &bars.kv_full[st], hb * 64,
+                        x.kvh, x.doc_start + j * kTile);
+          }
+          ++kvc;
+        }
+      }
+      if (!ok) {
+        if (units > 0) bwd_drain_wait(&bars.q_full, (units - 1) & 1);
+        for (int s = 0; s < 2; ++s)
+          if (kv_uses[s] > 0) bwd_drain_wait(&bars.kv_full[s], (kv_uses[s] - 1) & 1);
+      }
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kBwdThreads);
+  } else if (warp == kBwdMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t idesc_q = idesc_bf16_f32(128, D, 1);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), L::kHalfBytes, 1024);
+      uint32_t units = 0;
+      long long kvc = 0;  // key tiles issued so far (all units): stage, S buffer and barrier phases
+      bool ok = true;
+      // dQ += dS(t) K(t) for global tile t (its dS sits in S buffer t & 1, its K in stage t & 1)
+      auto issue_dq = [&](long long t, bool first_of_unit) -> bool {
+        if (!mbar_wait(&bars.p_full[t & 1], (t >> 1) & 1, abort_word, p.err, kErrDP)) return false;
+        if (first_of_unit && units > 0 &&
+            !mbar_wait(&bars.dq_empty, (units - 1) & 1, abort_word, p.err, kErrDDqE))
+          return false;
+        tc_fence_after();
+        const uint32_t a = tS0 + static_cast<uint32_t>(t & 1) * 128u;
+        const uint64_t b = dK_mn + static_cast<uint64_t>(t & 1) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tDQ, a + kk * 8 + (kk >= 4 ? 32 : 0), b + (static_cast<uint64_t>(kk * 2048) >> 4), idesc_q,
+                  (first_of_unit && kk == 0) ? 0u : 1u);
+        umma_commit(&bars.kv_empty[t & 1]);
+        return true;
+      };
+      for (long long k = 0; ok; ++k) {
+        const long long u = bwd_unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const DqUnit x = dq_unit(p, u);
+        ok = mbar_wait(&bars.q_full, units & 1, abort_word, p.err, kErrDQ);
+        if (!ok) break;
+        for (int j = 0; j < x.ntk && ok; ++j) {
+          const int st = static_cast<int>(kvc & 1);
+          ok = mbar_wait(&bars.kv_full[st], (kvc >> 1) & 1, abort_word, p.err, kErrDKv);
+          if (!ok) break;
+          // S(j) into buffer st: its previous dS was read by a dQ MMA issued earlier
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+            umma_ss(tS0 + st * 128u, dQ_k + off, dK_k + st * kTileUnits + off, idesc_s, kk > 0);
+          }
+          // dP(j) once the compute warps have read dP(j-1)
+          if (kvc > 0) {
+            ok = mbar_wait(&bars.dp_free, (kvc - 1) & 1, abort_word, p.err, kErrDDp);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+            umma_ss(tDP, dDO_k + off, dV_k + st * kTileUnits + off, idesc_s, kk > 0);
+          }
+          umma_commit(&bars.s_full);
+          if (j == x.ntk - 1) umma_commit(&bars.q_empty);  // Q and dO are read by then
+          // dQ of the previous tile of this unit
+          if (j > 0) ok = issue_dq(kvc - 1, j == 1);
+          ++kvc;
+        }
+        if (ok) ok = issue_dq(kvc - 1, x.ntk == 1);
+        if (ok) umma_commit(&bars.dq_full);
+        ++units;
+      }
+      umma_commit(&bars.drain);
+      bwd_drain_wait(&bars.drain, 0);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier_sync(1, kBwdThreads);
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warps (thread = query row)
+    const int qt = warp & 3, hf = warp >> 2;
+    const int r = qt * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qt * 32) << 16;
+    long long tg = 0;
+    uint32_t units = 0;
+    bool ok = true;
+    for (long long k = 0; ok; ++k) {
+      const long long u = bwd_unit_index(k, cta, nctas);
+      if (u >= total_units) break;
+      const DqUnit x = dq_unit(p, u);
+      const int q_local = x.i * kTile + r;
+      const bool row_ok = r < x.q_rows;
+      const long long tok = static_cast<long long>(x.q_row0) + r;
+      const float lse2 = row_ok ? __ldg(p.lse + static_cast<long long>(x.h) * p.T + tok) * 1.4426950408889634f : 0.f;
+      const float dlr = row_ok ? __ldg(p.dl + static_cast<long long>(x.h) * p.T + tok) : 0.f;
+      for (int j = 0; j < x.ntk; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, tg & 1, abort_word, p.err, kErrDS));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tS0 + static_cast<uint32_t>(tg & 1) * 128u;
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(tS + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(tS + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_ld32(tDP + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(dpv));
+        tmem_ld32(tDP + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dpv + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dp_free);
+        // key column c (doc-local key j*128 + 64 hf + c) is allowed iff it is <= q_local
+        const int c_hi = row_ok ? q_local - (j * kTile + hf * 64) + 1 : 0;  // allowed: c < c_hi
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float dd[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int c = cc * 32 + e + t;
+              const float pe = c < c_hi ? ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2)) : 0.f;
+              dd[t] = pe * (__uint_as_float(dpv[c]) - dlr) * p.scale;
+            }
+            pk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+          }
+          tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[tg & 1]);
+        ++tg;
+      }
+      if (!ok) break;
+      // ---- dQ of the unit -> bf16 rows
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, units & 1, abort_word, p.err, kErrDDq));
+      if (!ok) break;
+      tc_fence_after();
+      __nv_bfloat16* out = p.dq + (tok * p.hq + x.h) * static_cast<long long>(D) + hf * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDQ + lane_off + hf * (D / 2) + c * 32, v);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint4 w[4];
+          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) wp[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d4[e] = w[e];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dq_empty);
+      ++units;
+    }
+    named_barrier_sync(1, kBwdThreads);
+  } else {
+    named_barrier_sync(1, kBwdThreads);
   }
 }
 
@@ -546,33 +786,17 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ o, const __nv_bflo
   }
 }
 
-// fp32 dQ workspace -> bf16 dq (8 elements per thread).
-__global__ void k_bwd_dq_convert(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    uint4 w;
-    w.x = pack_bf16x2(a.x, a.y);
-    w.y = pack_bf16x2(a.z, a.w);
-    w.z = pack_bf16x2(b.x, b.y);
-    w.w = pack_bf16x2(b.z, b.w);
-    reinterpret_cast<uint4*>(dq)[i] = w;
-  }
-}
-
 size_t bwd_align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-void bwd_workspace(const hdp_plan_s* plan, int hq, int d, size_t* acc_bytes, size_t* total) {
+void bwd_workspace(const hdp_plan_s* plan, int hq, size_t* total) {
   const size_t T = static_cast<size_t>(plan->v.total_tokens);
-  *acc_bytes = bwd_align256(T * hq * d * sizeof(float));
-  *total = *acc_bytes + bwd_align256(T * hq * sizeof(float));
+  *total = bwd_align256(T * hq * sizeof(float));  // D = rowsum(dout * o)
 }
 
 template <int D>
 hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dout, int hq, int hkv, float scale, float* dq_acc, float* dl,
-                        void* dq, void* dk, void* dv, cudaStream_t st) {
+                        const float* lse, const void* dout, int hq, int hkv, float scale, float* dl, void* dq,
+                        void* dk, void* dv, cudaStream_t st) {
   const long long T = plan->v.total_tokens;
   if (T == 0) return HDP_OK;
   CUtensorMap mq, mk, mv, mdo;
@@ -581,18 +805,15 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   if ((r = make_bf16_tile_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_bf16_tile_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_bf16_tile_map(&mdo, dout, T, hq, D)) != HDP_OK) return r;
-  CUtensorMap mdq;
-  if ((r = make_f32_reduce_map(&mdq, dq_acc, T, hq, D)) != HDP_OK) return r;
   int dev = 0, sms = 0;
   HDP_CUDA_TRY(cudaGetDevice(&dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  // D = rowsum(dO * O) and a zeroed dQ accumulator
+  // D = rowsum(dO * O)
   const long long rows = T * hq;
   k_bwd_delta<D><<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dl, rows, hq, T);
   note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
-  HDP_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), st));
   BwdParams prm{};
   prm.tiles = plan->v.tiles_fused;
   prm.ntiles = plan->v.num_tiles_fused;
@@ -604,23 +825,31 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.lse = lse;
   prm.dl = dl;
-  prm.dq_acc = dq_acc;
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.err = device_error_word();
   if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
-  const long long units = prm.ntiles * hkv;
-  const int grid = static_cast<int>(units < sms ? units : sms);
-  const int smem = BwdSmem<D>::kBytes + 1024;
-  HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, mdq, prm);
-  note_launch();
-  HDP_CUDA_TRY(cudaGetLastError());
-  const long long n8 = rows * D / 8;
-  const int cgrid = static_cast<int>(n8 / 256 + 1 < 8L * sms ? n8 / 256 + 1 : 8L * sms);
-  k_bwd_dq_convert<<<cgrid, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
-  note_launch();
-  HDP_CUDA_TRY(cudaGetLastError());
+  // dK, dV: one unit per (key tile, kv head)
+  {
+    const long long units = prm.ntiles * hkv;
+    const int grid = static_cast<int>(units < sms ? units : sms);
+    const int smem = BwdSmem<D>::kBytes + 1024;
+    HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);
+    note_launch();
+    HDP_CUDA_TRY(cudaGetLastError());
+  }
+  // dQ: one unit per (query tile, query head)
+  {
+    const long long units = prm.ntiles * hq;
+    const int grid = static_cast<int>(units < sms ? units : sms);
+    const int smem = DqSmem<D>::kBytes + 1024;
+    HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    k_attn_bwd_dq<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);
+    note_launch();
+    HDP_CUDA_TRY(cudaGetLastError());
+  }
   return HDP_OK;
 }
 
@@ -633,8 +862,7 @@ extern "C" hdp_status_t hdp_attention_bwd_workspace_bytes(hdp_plan_t plan, int32
   if (!plan || !bytes) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd_workspace_bytes: NULL argument");
   if (hq < 1 || d < 1)
     return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd_workspace_bytes: hq, d must be >= 1");
-  size_t acc = 0;
-  bwd_workspace(plan, hq, d, &acc, bytes);
+  bwd_workspace(plan, hq, bytes);
   return HDP_OK;
 }
 
@@ -654,16 +882,15 @@ extern "C" hdp_status_t hdp_attention_bwd(hdp_plan_t plan, const void* q, const 
                         reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
   if (mis & 15)
     return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: q, k, v, o, dout, dq, dk, dv must be 16-byte aligned");
-  size_t acc = 0, need = 0;
-  bwd_workspace(plan, hq, d, &acc, &need);
+  size_t need = 0;
+  bwd_workspace(plan, hq, &need);
   if (!workspace || workspace_bytes < need)
     return fail(HDP_ERR_INVALID_ARGUMENT,
                 "hdp_attention_bwd: workspace too small (need " + std::to_string(need) + " bytes)");
   if (reinterpret_cast<uintptr_t>(workspace) & 255)
     return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_bwd: workspace must be 256-byte aligned");
-  float* dq_acc = static_cast<float*>(workspace);
-  float* dl = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  float* dl = static_cast<float*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dq_acc, dl, dq, dk, dv, st)
-                  : launch_bwd<64>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dq_acc, dl, dq, dk, dv, st);
+  return d == 128 ? launch_bwd<128>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dl, dq, dk, dv, st)
+                  : launch_bwd<64>(plan, q, k, v, o, lse, dout, hq, hkv, scale, dl, dq, dk, dv, st);
 }

@@ -95,15 +95,15 @@ def test_small_cases(lengths, hq, hkv, d, C):
     full_bwd_parity(lengths, hq, hkv, d, C, seed=len(lengths))
 
 
-def test_deterministic_dk_dv():
-    """dk and dv accumulate in one CTA's TMEM in a fixed order: bit-identical
-    across runs (dq uses atomics, so only its tolerance is checked)."""
+def test_deterministic():
+    """dq, dk and dv each accumulate in one CTA's TMEM in a fixed order, with
+    no atomics: bit-identical across runs."""
     lengths, hq, hkv, d = [700, 1300, 5], 8, 2, 128
     q, k, v, do = _inputs(lengths, hq, hkv, d, 9)
     a = run_bwd(q, k, v, do, lengths, 256)
     b = run_bwd(q, k, v, do, lengths, 256)
-    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
-    assert np.max(np.abs(a[0] - b[0])) <= 1e-2 * np.abs(a[0]).max()
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
 
 
 def _identities(w, q, k, v, do, dq, dk, dv):
@@ -170,7 +170,7 @@ def test_workspace_and_argument_checks():
     dl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
     with pkg.hdp_plan_create(dl, 256) as plan:
         need = pkg.hdp_attention_bwd_workspace_bytes(plan, 4, 128)
-        assert need >= 300 * 4 * 128 * 4 + 300 * 4 * 4
+        assert need >= 300 * 4 * 4  # D = rowsum(dout * o), fp32 [hq][T]
         q = torch.zeros(300, 4, 128, dtype=torch.bfloat16, device="cuda")
         k = torch.zeros(300, 2, 128, dtype=torch.bfloat16, device="cuda")
         lse = torch.zeros(4, 300, dtype=torch.float32, device="cuda")
