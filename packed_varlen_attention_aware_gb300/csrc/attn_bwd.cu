@@ -53,6 +53,10 @@ constexpr int kBwdThreads = 384;
 constexpr int kBwdProducer = 8;
 constexpr int kBwdMma = 9;
 constexpr uint32_t kDsBarrier = 2;  // named barrier of the eight compute warps
+// Launched at 168 registers a thread (384 x 168 = 64,512); setmaxnreg then
+// gives the compute warpgroups more: 2 x 128 x 200 + 128 x 104 = 64,512.
+constexpr int kBwdComputeRegs = 200;
+constexpr int kBwdControlRegs = 104;
 
 constexpr int kErrBKv = 0x201, kErrBQ = 0x202, kErrBS = 0x203, kErrBP = 0x204, kErrBDq = 0x205,
               kErrBDqE = 0x206, kErrBDkv = 0x207, kErrBDkvE = 0x208, kErrBKvE = 0x209, kErrBQE = 0x20a;
@@ -181,6 +185,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const uint32_t tDV = tmem, tDK = tmem + D, tS = tmem + 2 * D, tDP = tmem + 2 * D + 128;
 
+  if (warp >= 8) {
+  // control warpgroup: producer, MMA issuer, two idle warps; registers go to the compute warps
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdControlRegs));
   if (warp == kBwdProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -309,7 +316,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     named_barrier_sync(1, kBwdThreads);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
-  } else if (warp < 8) {
+  } else {
+    named_barrier_sync(1, kBwdThreads);  // idle warps
+  }
+  } else {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdComputeRegs));
     // ------------------------------------------------------------ compute warps 0-7
     // Warp w serves TMEM lane quarter qt = w % 4 (32 rows) and column half
     // hf = w / 4, so two warps share each scheduler and split every phase:
@@ -343,10 +354,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int q_local = i * kTile + t;
           const bool qv = q_local < x.doc_len;
           const long long tok = static_cast<long long>(x.doc_start) + q_local;
+          // stored as -LSE log2(e) and -D scale, the addends of the FMAs below
           if (threadIdx.x < 128)
-            lse2_s[t] = qv ? __ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
+            lse2_s[t] = qv ? -__ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
           else
-            dl_s[t] = qv ? __ldg(p.dl + static_cast<long long>(h) * p.T + tok) : 0.f;
+            dl_s[t] = qv ? -__ldg(p.dl + static_cast<long long>(h) * p.T + tok) * p.scale : 0.f;
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, it_global & 1, abort_word, p.err, kErrBS));
         if (named_barrier_or(kDsBarrier, 256, !ok)) {
@@ -367,26 +379,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(tDP + lane_off + c * 32, dpv);
           tmem_wait_ld();
           uint32_t pk_p[16], pk_ds[16];
-          const float4* l4 = reinterpret_cast<const float4*>(lse2_s + c * 32);
-          const float4* d4 = reinterpret_cast<const float4*>(dl_s + c * 32);
+          // P = 2^(S scale log2e - LSE log2e), dS = P (dP scale - D scale)
+          if (key_ok && c * 32 >= c_lo && c * 32 + 32 <= c_hi) {
+            // every query of the chunk is visible to this key: packed pairs
+            const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2), s2 = pack_f32x2(p.scale, p.scale);
+            const uint64_t* l2 = reinterpret_cast<const uint64_t*>(lse2_s + c * 32);
+            const uint64_t* d2 = reinterpret_cast<const uint64_t*>(dl_s + c * 32);
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 lv = l4[e4], dv = d4[e4];
-            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
-            float pp[4], dd[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int e = e4 * 4 + t;
-              const int col = c * 32 + e;
-              const bool allowed = key_ok && col >= c_lo && col < c_hi;
-              const float pe = allowed ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -la[t])) : 0.f;
-              pp[t] = pe;
-              dd[t] = pe * (__uint_as_float(dpv[e]) - da[t]) * p.scale;
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const uint64_t sp = (static_cast<uint64_t>(sv[2 * e2 + 1]) << 32) | sv[2 * e2];
+              const uint64_t dp = (static_cast<uint64_t>(dpv[2 * e2 + 1]) << 32) | dpv[2 * e2];
+              const uint64_t a = ffma_f32x2(sp, c2, l2[e2]);
+              const float p0 = ex2_approx(lo_f32(a)), p1 = ex2_approx(hi_f32(a));
+              const uint64_t ds = fmul_f32x2(pack_f32x2(p0, p1), ffma_f32x2(dp, s2, d2[e2]));
+              pk_p[e2] = pack_bf16x2(p0, p1);
+              pk_ds[e2] = pack_bf16x2(lo_f32(ds), hi_f32(ds));
             }
-            pk_p[e4 * 2] = pack_bf16x2(pp[0], pp[1]);
-            pk_p[e4 * 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-            pk_ds[e4 * 2] = pack_bf16x2(dd[0], dd[1]);
-            pk_ds[e4 * 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+          } else {
+            const float4* l4 = reinterpret_cast<const float4*>(lse2_s + c * 32);
+            const float4* d4 = reinterpret_cast<const float4*>(dl_s + c * 32);
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 lv = l4[e4], dv = d4[e4];
+              const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+              float pp[4], dd[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int e = e4 * 4 + t;
+                const int col = c * 32 + e;
+                const bool allowed = key_ok && col >= c_lo && col < c_hi;
+                const float pe = allowed ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, la[t])) : 0.f;
+                pp[t] = pe;
+                dd[t] = pe * fmaf(__uint_as_float(dpv[e]), p.scale, da[t]);
+              }
+              pk_p[e4 * 2] = pack_bf16x2(pp[0], pp[1]);
+              pk_p[e4 * 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+              pk_ds[e4 * 2] = pack_bf16x2(dd[0], dd[1]);
+              pk_ds[e4 * 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+            }
           }
           // P^T / dS^T (bf16 pairs) into this half's own columns, already
           // read: half hf owns S^T / dP^T columns [64 hf, 64 hf + 64), and
@@ -436,8 +466,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++units;
     }
     named_barrier_sync(1, kBwdThreads);
-  } else {
-    named_barrier_sync(1, kBwdThreads);  // idle warps
   }
 }
 
@@ -543,6 +571,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
 
+  if (warp >= 8) {
+  // control warpgroup: producer, MMA issuer, two idle warps; registers go to the compute warps
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdControlRegs));
   if (warp == kBwdProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -667,7 +698,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     named_barrier_sync(1, kBwdThreads);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
-  } else if (warp < 8) {
+  } else {
+    named_barrier_sync(1, kBwdThreads);
+  }
+  } else {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdComputeRegs));
     // ------------------------------------------------------------ compute warps (thread = query row)
     const int qt = warp & 3, hf = warp >> 2;
     const int r = qt * 32 + lane;
@@ -684,6 +719,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const long long tok = static_cast<long long>(x.q_row0) + r;
       const float lse2 = row_ok ? __ldg(p.lse + static_cast<long long>(x.h) * p.T + tok) * 1.4426950408889634f : 0.f;
       const float dlr = row_ok ? __ldg(p.dl + static_cast<long long>(x.h) * p.T + tok) : 0.f;
+      const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2), s2 = pack_f32x2(p.scale, p.scale);
+      const uint64_t nl2 = pack_f32x2(-lse2, -lse2), nd2 = pack_f32x2(-dlr * p.scale, -dlr * p.scale);
       for (int j = 0; j < x.ntk; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, tg & 1, abort_word, p.err, kErrDS));
         if (!ok) break;
@@ -703,16 +740,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];
+          if (c_hi >= cc * 32 + 32) {
+            // every key of the chunk is visible to this query: packed pairs
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float dd[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int c = cc * 32 + e + t;
-              const float pe = c < c_hi ? ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2)) : 0.f;
-              dd[t] = pe * (__uint_as_float(dpv[c]) - dlr) * p.scale;
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const int c = cc * 32 + 2 * e2;
+              const uint64_t sp = (static_cast<uint64_t>(sv[c + 1]) << 32) | sv[c];
+              const uint64_t dp = (static_cast<uint64_t>(dpv[c + 1]) << 32) | dpv[c];
+              const uint64_t a = ffma_f32x2(sp, c2, nl2);
+              const float p0 = ex2_approx(lo_f32(a)), p1 = ex2_approx(hi_f32(a));
+              const uint64_t ds = fmul_f32x2(pack_f32x2(p0, p1), ffma_f32x2(dp, s2, nd2));
+              pk[e2] = pack_bf16x2(lo_f32(ds), hi_f32(ds));
             }
-            pk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float dd[2];
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const int c = cc * 32 + e + t;
+                const float pe = c < c_hi ? ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2)) : 0.f;
+                dd[t] = pe * (__uint_as_float(dpv[c]) - dlr) * p.scale;
+              }
+              pk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+            }
           }
           tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk);
         }
@@ -748,8 +799,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bars.dq_empty);
       ++units;
     }
-    named_barrier_sync(1, kBwdThreads);
-  } else {
     named_barrier_sync(1, kBwdThreads);
   }
 }
