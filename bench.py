@@ -144,6 +144,27 @@ def dist_setup():
     return ws, rank, local
 
 
+def aggregate_over_ranks(times, flops, ws, device):
+    """Replicas (weak scaling: every rank runs its own micro-batch, no data-path
+    collective): the job's times are the slowest rank's, its useful FLOPs the
+    sum over ranks.  Returns (list of max times, summed FLOPs)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    f = torch.tensor([float(flops)], dtype=torch.float64, device=device)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return t.tolist(), f.item()
+
+
+def job_throughput(job_flops: float, steps: int, ms: float) -> float:
+    """Whole-job useful TFLOP/s: the FLOPs every rank did in `steps` steps over
+    the slowest rank's time for them."""
+    return job_flops * steps / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(w, q, k, v, seconds: float, seed: int):
@@ -383,13 +404,7 @@ def our_arm(args, ws, rank, local):
     h2d = in_bytes + lh.numel() * 4
     d2h = oh.numel() * 2 + lseh.numel() * 4 + fh.numel() * 8
 
-    times = torch.tensor([ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
-    total_flops = torch.tensor([float(flops_step)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-        dist.all_reduce(total_flops, op=dist.ReduceOp.SUM)
-    ms, e2e_ms, attn_ms_max = times.tolist()
-    job_flops = total_flops.item()
+    (ms, e2e_ms, attn_ms_max), job_flops = aggregate_over_ranks([ms, e2e_ms, attn_ms], flops_step, ws, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -400,7 +415,7 @@ def our_arm(args, ws, rank, local):
     if rank == 0:
         peaks, src = load_peaks()
         achieved = flops_step / (attn_ms * 1e-3) / 1e12
-        value = job_flops * args.steps / (ms * 1e-3) / 1e12
+        value = job_throughput(job_flops, args.steps, ms)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -413,7 +428,7 @@ def our_arm(args, ws, rank, local):
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "attn_ms": attn_ms, "traffic": traffic_from_profile()},
             "cpu_baseline": cpu,
-            "e2e": {"value": job_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": job_throughput(job_flops, args.steps, e2e_ms), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
                     "pipeline": "step i+1 upload and step i-1 download overlap step i compute"},
             "gpu_launches": launches,
