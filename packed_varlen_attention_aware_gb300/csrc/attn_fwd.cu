@@ -47,14 +47,15 @@ namespace {
 // 12 warps = 3 warpgroups: two softmax warpgroups and one for the producer
 // (warp 8), the MMA issuer (warp 9), its waiter (warp 10) and an idle warp.
 // Launched at 168 registers a thread (384 x 168 = 64,512); setmaxnreg then moves registers to
-// the softmax warpgroups: 2 x 128 x 192 + 128 x 120 = 64,512.
+// the softmax warpgroups: 2 x 128 x 176 + 128 x 152 = 64,512 (the MMA
+// issuer's straight-line code needs the control share).
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kWaitWarp = 10;
 constexpr uint32_t kHandoffBarrier = 2;  // named barrier between the waiter and MMA warps
-constexpr int kSoftmaxRegs = 192;
-constexpr int kControlRegs = 120;
+constexpr int kSoftmaxRegs = 176;
+constexpr int kControlRegs = 152;
 constexpr int kStages = 2;  // K and V ring depth
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
@@ -299,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
     constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+    const uint64_t dK1 = dK + kTileUnits, dV1 = dV + kTileUnits;
     auto issue_qk = [&](int s, int kst) {
-      const uint64_t qd = dQ + s * kTileUnits, kd = dK + kst * kTileUnits;
+      const uint64_t qd = dQ + s * kTileUnits, kd = kst ? dK1 : dK;
       umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
 #pragma unroll
       for (int kk = 1; kk < D / 16; ++kk) {
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars.s_full[s]);
     };
     auto issue_pv = [&](int s, int vst, bool accumulate) {
-      const uint64_t vd = dV + vst * kTileUnits;
+      const uint64_t vd = vst ? dV1 : dV;
       if (accumulate)
         umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
       else
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
     };
     uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
-    long long kuse = 0, vuse = 0, g = 0;
+    long long g = 0;
     bool ok = true;  // the waiter's own waits so far
     auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
       if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code);
@@ -337,7 +339,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return !failed;
     };
+    // K and V stages advance together (n of each per unit), so one parity c
+    // per unit fixes them: P.V(j) reads V stage c ^ (j & 1), S(j+1) K stage
+    // c ^ 1 ^ (j & 1).  The steady key tiles are unrolled by two with those
+    // stages as constants, and the last two tiles are peeled, so the issuing
+    // thread runs straight-line code: per-MMA index arithmetic or commit
+    // branches inside its one-lane region cost it tens of cycles a MMA.
     bool alive = true;
+    // key tile j of the unit; kind 0: steady (j < n - 2), 1: j = n - 2 (Q is
+    // free after its S), 2: j = n - 1 (the unit's last P.V)
+    auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind) -> bool {
+      for (int s = 0; s < nslots; ++s) {
+        // handoff: (slot 0) the group holding V(j) and K(j+1); P_s(j)
+        // written and O_s rescaled by the softmax warps; and, before the
+        // first P.V of a unit overwrites O_s, the previous epilogue's read
+        if (waiter) {
+          if (s == 0) wait_group(kErrVFull);
+          wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);
+          if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
+        }
+        if (s == 0) ++g;
+        ++p_uses[s];
+        if (!handoff()) return false;
+        if (issuer) {
+          issue_pv(s, vs, j > 0);
+          if (kind == 2) {
+            umma_commit(&bars.o_full[s]);
+          } else {
+            issue_qk(s, ks);
+            if (kind == 1) umma_commit(&bars.q_empty[s]);
+          }
+        }
+      }
+      if (issuer) {
+        if (kind != 2) umma_commit(&bars.k_empty[ks]);
+        umma_commit(&bars.v_empty[vs]);
+      }
+      return true;
+    };
+    int c = 0;  // stage parity at the start of a unit
     for (long long k = 0; alive; ++k) {
       const long long u = unit_index(k, cta, nctas);
       if (u >= total_units) break;
@@ -352,53 +392,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < nslots; ++s) ++q_uses[s];
       ++g;
       if (!handoff()) break;
-      int kst = static_cast<int>(kuse % kStages);
       if (issuer) {
         for (int s = 0; s < nslots; ++s) {
-          issue_qk(s, kst);
+          issue_qk(s, c);
           if (n == 1) umma_commit(&bars.q_empty[s]);
         }
-        umma_commit(&bars.k_empty[kst]);
+        umma_commit(&bars.k_empty[c]);
       }
-      ++kuse;
-      for (int j = 0; j < n && alive; ++j) {
-        const int vst = static_cast<int>(vuse % kStages);
-        const bool more = j + 1 < n;
-        kst = static_cast<int>(kuse % kStages);
-        for (int s = 0; s < nslots; ++s) {
-          // handoff: (slot 0) the group holding V(j) and K(j+1); P_s(j)
-          // written and O_s rescaled by the softmax warps; and, before the
-          // first P.V of a unit overwrites O_s, the previous epilogue's read
-          if (waiter) {
-            if (s == 0) wait_group(kErrVFull);
-            wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);
-            if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
-          }
-          if (s == 0) ++g;
-          ++p_uses[s];
-          if (!handoff()) {
-            alive = false;
-            break;
-          }
-          if (issuer) {
-            issue_pv(s, vst, j > 0);
-            if (!more) umma_commit(&bars.o_full[s]);
-            if (more) {
-              issue_qk(s, kst);
-              if (j + 2 == n) umma_commit(&bars.q_empty[s]);
-            }
-          }
-        }
-        if (!alive) break;
-        if (more) {
-          if (issuer) umma_commit(&bars.k_empty[kst]);
-          ++kuse;
-        }
-        if (issuer) umma_commit(&bars.v_empty[vst]);
-        ++vuse;
+      int j = 0;
+      if (c == 0) {
+        for (; j + 1 < n - 2 && alive; j += 2) alive = tile(x, nslots, j, 0, 1, 0) && tile(x, nslots, j + 1, 1, 0, 0);
+      } else {
+        for (; j + 1 < n - 2 && alive; j += 2) alive = tile(x, nslots, j, 1, 0, 0) && tile(x, nslots, j + 1, 0, 1, 0);
       }
-      if (alive)
-        for (int s = 0; s < nslots; ++s) ++units_done[s];
+      for (; j < n - 2 && alive; ++j) alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0);
+      if (alive && n >= 2) {
+        alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 1);
+        ++j;
+      }
+      if (alive) alive = tile(x, nslots, j, c ^ (j & 1), 0, 2);
+      if (!alive) break;
+      c ^= n & 1;
+      for (int s = 0; s < nslots; ++s) ++units_done[s];
     }
     if (issuer) {
       // drain every MMA this thread issued before TMEM is released
