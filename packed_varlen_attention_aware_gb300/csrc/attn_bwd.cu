@@ -45,7 +45,6 @@
 namespace hdp {
 
 hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, int heads, int d);
-hdp_status_t make_f32_reduce_map(CUtensorMap* m, void* base, long long T, int heads, int d);
 
 namespace {
 

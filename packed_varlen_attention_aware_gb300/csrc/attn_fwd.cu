@@ -636,20 +636,6 @@ hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, i
   return make_map(m, base, T, heads, d);
 }
 
-// fp32 [T][heads][d] viewed as (d, heads, T) for reduce-adds from shared
-// memory: box = 32 columns (128 bytes) x 1 head x 32 rows, 128-byte swizzle.
-hdp_status_t make_f32_reduce_map(CUtensorMap* m, void* base, long long T, int heads, int d) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return fail(HDP_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(heads) * d * 4};
-  cuuint32_t box[3] = {32, 1, 32};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(HDP_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (" + std::to_string(r) + ")");
-  return HDP_OK;
-}
 
 namespace {
 
