@@ -53,31 +53,40 @@ constexpr int kBwdProducer = 8;
 constexpr int kBwdMma = 9;
 constexpr uint32_t kDsBarrier = 2;  // named barrier of the eight compute warps
 // Launched at 168 registers a thread (384 x 168 = 64,512); setmaxnreg then
-// gives the compute warpgroups more: 2 x 128 x 200 + 128 x 104 = 64,512.
+// gives the compute warpgroups more: 2 x 128 x 200 + 128 x 104 = 64,512
+// (dQ pass, and the dK/dV pass at d = 64), 2 x 128 x 208 + 128 x 88 =
+// 64,512 (dK/dV pass at d = 128, whose compute warps hold P and dP rows).
 constexpr int kBwdComputeRegs = 200;
 constexpr int kBwdControlRegs = 104;
+template <int D>
+struct KvRegs {
+  static constexpr int kCompute = D == 128 ? 208 : kBwdComputeRegs;
+  static constexpr int kControl = D == 128 ? 88 : kBwdControlRegs;
+  static_assert(2 * 128 * kCompute + 128 * kControl == 384 * 168, "register split must use the launch's pool");
+};
 
-constexpr int kErrBKv = 0x201, kErrBQ = 0x202, kErrBS = 0x203, kErrBP = 0x204, kErrBDq = 0x205,
-              kErrBDqE = 0x206, kErrBDkv = 0x207, kErrBDkvE = 0x208, kErrBKvE = 0x209, kErrBQE = 0x20a;
+constexpr int kErrBKv = 0x201, kErrBQ = 0x202, kErrBS = 0x203, kErrBP = 0x204, kErrBDkv = 0x207, kErrBDkvE = 0x208,
+              kErrBKvE = 0x209, kErrBQE = 0x20a;
 
 template <int D>
 struct BwdSmem {
   static constexpr int kTileBytes = kTile * D * 2;  // 128 x D bf16
   static constexpr int kHalfBytes = kTile * 64 * 2;
+  static constexpr int kQStages = 3;                // Q(i) is read last by dK(i): keep two tiles in flight
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;           // 2 stages
-  static constexpr int kDO = kQ + 2 * kTileBytes;      // 2 stages
-  static constexpr int kLse = kDO + 2 * kTileBytes;    // 128 fp32: LSE * log2(e) of the tile's queries
-  static constexpr int kDl = kLse + kTile * 4;         // 128 fp32: D of the tile's queries
-  static constexpr int kBar = kDl + kTile * 4;
+  static constexpr int kQ = kV + kTileBytes;                    // 3 stages
+  static constexpr int kDO = kQ + kQStages * kTileBytes;        // 2 stages
+  static constexpr int kLse = kDO + 2 * kTileBytes;  // 128 fp32: -LSE log2(e) of the tile's queries
+  static constexpr int kDl = kLse + kTile * 4;       // 2 x 128 fp32: -D scale, by tile parity
+  static constexpr int kBar = kDl + 2 * kTile * 4;
   static constexpr int kBytes = kBar + 256;
 };
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, p_full, dkv_full, dkv_empty, drain;
+  uint64_t q_full[3], q_empty[3], do_full[2], do_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort_word;
 };
@@ -156,12 +165,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
     mbar_init(&bars.kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::kQStages; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.do_full[s], 1);
+      mbar_init(&bars.do_empty[s], 1);
+    }
     mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.p_full, 8);
+    mbar_init(&bars.ds_full, 8);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.dkv_empty, 8);
     mbar_init(&bars.drain, 1);
@@ -186,13 +201,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp >= 8) {
   // control warpgroup: producer, MMA issuer, two idle warps; registers go to the compute warps
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdControlRegs));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(KvRegs<D>::kControl));
   if (warp == kBwdProducer) {
     // ------------------------------------------------------------ TMA producer
+    // Q of tile g goes to stage g % 3, dO to stage g % 2 (g counts the
+    // query tiles of all units of this CTA); K and V once per unit.
     if (lane == 0) {
-      uint32_t q_uses[2] = {0, 0};
-      long long it_global = 0;
-      uint32_t units = 0;
+      int qs = 0;
+      long long g = 0, q_armed = 0;    // tiles whose dO / Q loads were issued
+      uint32_t units = 0, qround = 0;  // qround: completed passes over the Q stages
       bool ok = true;
       for (long long k = 0; ok; ++k) {
         const long long u = bwd_unit_index(k, cta, nctas);
@@ -212,29 +229,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; it < x.iters; ++it) {
           int h, i;
           bwd_iter(p, x, it, &h, &i);
-          const int st = static_cast<int>(it_global & 1);
-          if (q_uses[st] > 0 && !mbar_wait(&bars.q_empty[st], (q_uses[st] - 1) & 1, abort_word, p.err, kErrBQE)) {
+          const int q_row0 = x.doc_start + i * kTile;
+          if (qround > 0 && !mbar_wait(&bars.q_empty[qs], (qround - 1) & 1, abort_word, p.err, kErrBQE)) {
+            q_armed = g;
             ok = false;
             break;
           }
-          ++q_uses[st];
-          const int q_row0 = x.doc_start + i * kTile;
-          mbar_arrive_expect_tx(&bars.q_full[st], 2 * L::kTileBytes);
+          mbar_arrive_expect_tx(&bars.q_full[qs], L::kTileBytes);
 #pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb) {
-            tma_load_3d(smem + L::kQ + st * L::kTileBytes + hb * L::kHalfBytes, &tmQ, &bars.q_full[st], hb * 64, h,
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem + L::kQ + qs * L::kTileBytes + hb * L::kHalfBytes, &tmQ, &bars.q_full[qs], hb * 64, h,
                         q_row0);
-            tma_load_3d(smem + L::kDO + st * L::kTileBytes + hb * L::kHalfBytes, &tmDO, &bars.q_full[st], hb * 64,
-                        h, q_row0);
+          const int ds = static_cast<int>(g & 1);
+          if (g >= 2 && !mbar_wait(&bars.do_empty[ds], ((g >> 1) - 1) & 1, abort_word, p.err, kErrBQE)) {
+            q_armed = g + 1;
+            ok = false;
+            break;
           }
-          ++it_global;
+          mbar_arrive_expect_tx(&bars.do_full[ds], L::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem + L::kDO + ds * L::kTileBytes + hb * L::kHalfBytes, &tmDO, &bars.do_full[ds], hb * 64,
+                        h, q_row0);
+          if (++qs == L::kQStages) {
+            qs = 0;
+            ++qround;
+          }
+          q_armed = ++g;
         }
       }
       if (!ok) {
-        // every armed barrier completes once its bytes land
+        // every armed barrier completes once its bytes land: stage s of Q
+        // was armed by the tiles t < q_armed with t % 3 == s, of dO by the
+        // tiles t < g with t % 2 == s
         if (units > 0) bwd_drain_wait(&bars.kv_full, (units - 1) & 1);
-        for (int s = 0; s < 2; ++s)
-          if (q_uses[s] > 0) bwd_drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
+        for (int s = 0; s < L::kQStages; ++s) {
+          const long long uses = (q_armed + L::kQStages - 1 - s) / L::kQStages;
+          if (uses > 0) bwd_drain_wait(&bars.q_full[s], static_cast<uint32_t>(uses - 1) & 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+          const long long uses = (g + 1 - s) / 2;
+          if (uses > 0) bwd_drain_wait(&bars.do_full[s], static_cast<uint32_t>(uses - 1) & 1);
+        }
       }
     }
     __syncwarp();
@@ -242,6 +278,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     named_barrier_sync(1, kBwdThreads);
   } else if (warp == kBwdMma) {
     // ------------------------------------------------------------ MMA issuer
+    // Issue order, tile g then g + 1:
+    //   ... S(g) dP(g) | P(g) | dV(g) S(g+1) | dS(g) | dK(g) dP(g+1) | P(g+1) | ...
+    // so the tensor pipe computes dV(g) and S(g+1) while the compute warps
+    // turn dP(g) into dS(g), and dK(g), dP(g+1) while they turn S(g+1) into
+    // P(g+1).  S(g+1) overwrites the columns that hold P(g), and dP(g+1)
+    // those of dS(g): the pipe executes in issue order, so the MMA that
+    // reads them has already run.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);   // K-major A and B
       constexpr uint32_t idesc_kv = idesc_bf16_f32(128, D, 1);    // A from TMEM, B MN-major
@@ -252,60 +295,107 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
       const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + L::kQ), L::kHalfBytes, 1024);
       const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + L::kDO), L::kHalfBytes, 1024);
-      long long it_global = 0;
-      uint32_t units = 0;
-      bool ok = true;
-      for (long long k = 0; ok; ++k) {
-        const long long u = bwd_unit_index(k, cta, nctas);
-        if (u >= total_units) break;
-        const BwdUnit x = bwd_unit(p, u);
-        ok = mbar_wait(&bars.kv_full, units & 1, abort_word, p.err, kErrBKv);
-        if (!ok) break;
-        for (int it = 0; it < x.iters && ok; ++it) {
-          const int st = static_cast<int>(it_global & 1);
-          ok = mbar_wait(&bars.q_full[st], (it_global >> 1) & 1, abort_word, p.err, kErrBQ);
-          if (!ok) break;
-          const uint64_t qk = dQ_k + st * kTileUnits, dok = dDO_k + st * kTileUnits;
-          // S^T = K_j Q_i^T
+      // S^T = K_j Q_g^T into tS
+      auto issue_s = [&](int qs) {
+        const uint64_t qk = dQ_k + static_cast<uint64_t>(qs) * kTileUnits;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
-            umma_ss(tS, dK_k + off, qk + off, idesc_s, kk > 0);
-          }
-          // dP^T = V_j dO_i^T (dS^T of the previous tile, in these columns, was
-          // read by its dK MMA, issued earlier)
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
-            umma_ss(tDP, dV_k + off, dok + off, idesc_s, kk > 0);
-          }
-          umma_commit(&bars.s_full);
-          // P^T, dS^T in TMEM and dS in smem from the dS warps
-          ok = mbar_wait(&bars.p_full, it_global & 1, abort_word, p.err, kErrBP);
-          if (ok && it == 0 && units > 0)
-            ok = mbar_wait(&bars.dkv_empty, (units - 1) & 1, abort_word, p.err, kErrBDkvE);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t first = it == 0 ? 0u : 1u;
-          const uint64_t qmn = dQ_mn + st * kTileUnits, domn = dDO_mn + st * kTileUnits;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
-            umma_ts(tDV, tS + kk * 8 + (kk >= 4 ? 32 : 0), domn + off, idesc_kv, kk > 0 ? 1u : first);
-          }
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(kk * 2048) >> 4;
-            umma_ts(tDK, tDP + kk * 8 + (kk >= 4 ? 32 : 0), qmn + off, idesc_kv, kk > 0 ? 1u : first);
-          }
-          umma_commit(&bars.q_empty[st]);
-          if (it == x.iters - 1) {
-            umma_commit(&bars.kv_empty);
-            umma_commit(&bars.dkv_full);
-          }
-          ++it_global;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+          umma_ss(tS, dK_k + off, qk + off, idesc_s, kk > 0);
         }
-        ++units;
+        umma_commit(&bars.s_full);
+      };
+      // dP^T = V_j dO_g^T into tDP
+      auto issue_dp = [&](int ds) {
+        const uint64_t dok = dDO_k + static_cast<uint64_t>(ds) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+          umma_ss(tDP, dV_k + off, dok + off, idesc_s, kk > 0);
+        }
+        umma_commit(&bars.dp_full);
+      };
+      long long g = 0;                 // current tile: S(g), dP(g) issued
+      int qs = 0, qs_next = 1;         // Q stages of tiles g and g + 1
+      uint32_t units = 0;              // index of the current unit
+      long long k = 0;
+      long long u = bwd_unit_index(0, cta, nctas);
+      bool ok = u < total_units;
+      BwdUnit x{};
+      int it = 0;
+      if (ok) {
+        x = bwd_unit(p, u);
+        ok = mbar_wait(&bars.kv_full, 0, abort_word, p.err, kErrBKv) &&
+             mbar_wait(&bars.q_full[0], 0, abort_word, p.err, kErrBQ);
+        if (ok) issue_s(0);
+        if (ok) ok = mbar_wait(&bars.do_full[0], 0, abort_word, p.err, kErrBQ);
+        if (ok) {
+          issue_dp(0);
+          if (x.iters == 1) umma_commit(&bars.kv_empty);
+        }
+      }
+      while (ok) {
+        const bool first = it == 0, last = it == x.iters - 1;
+        const int ds = static_cast<int>(g & 1);
+        // dV += P^T dO_g, once the compute warps have written P(g)
+        ok = mbar_wait(&bars.p_full, g & 1, abort_word, p.err, kErrBP);
+        if (ok && first && units > 0)
+          ok = mbar_wait(&bars.dkv_empty, (units - 1) & 1, abort_word, p.err, kErrBDkvE);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t domn = dDO_mn + static_cast<uint64_t>(ds) * kTileUnits;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts(tDV, tS + kk * 8 + (kk >= 4 ? 32 : 0), domn + (static_cast<uint64_t>(kk * 2048) >> 4), idesc_kv,
+                    (kk > 0 || !first) ? 1u : 0u);
+        }
+        umma_commit(&bars.do_empty[ds]);
+        // the next tile: same unit, or the first tile of the next unit
+        bool has_next = true, next_new_unit = false;
+        BwdUnit xn = x;
+        if (last) {
+          const long long un = bwd_unit_index(k + 1, cta, nctas);
+          has_next = un < total_units;
+          next_new_unit = true;
+          if (has_next) xn = bwd_unit(p, un);
+        }
+        if (has_next) {
+          if (next_new_unit) ok = mbar_wait(&bars.kv_full, (units + 1) & 1, abort_word, p.err, kErrBKv);
+          if (ok) ok = mbar_wait(&bars.q_full[qs_next], ((g + 1) / L::kQStages) & 1, abort_word, p.err, kErrBQ);
+          if (!ok) break;
+          issue_s(qs_next);
+        }
+        // dK += dS^T Q_g, once the compute warps have written dS(g)
+        ok = mbar_wait(&bars.ds_full, g & 1, abort_word, p.err, kErrBP);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t qmn = dQ_mn + static_cast<uint64_t>(qs) * kTileUnits;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts(tDK, tDP + kk * 8 + (kk >= 4 ? 32 : 0), qmn + (static_cast<uint64_t>(kk * 2048) >> 4), idesc_kv,
+                    (kk > 0 || !first) ? 1u : 0u);
+        }
+        umma_commit(&bars.q_empty[qs]);
+        if (last) umma_commit(&bars.dkv_full);
+        if (!has_next) break;
+        ok = mbar_wait(&bars.do_full[ds ^ 1], ((g + 1) >> 1) & 1, abort_word, p.err, kErrBQ);
+        if (!ok) break;
+        issue_dp(ds ^ 1);
+        // K and V of a unit are read last by the S and dP of its last tile
+        if (next_new_unit) {
+          x = xn;
+          ++k;
+          ++units;
+          it = 0;
+        } else {
+          ++it;
+        }
+        if (it == x.iters - 1) umma_commit(&bars.kv_empty);
+        ++g;
+        qs = qs_next;
+        qs_next = qs_next == L::kQStages - 1 ? 0 : qs_next + 1;
       }
       umma_commit(&bars.drain);
       bwd_drain_wait(&bars.drain, 0);
@@ -319,19 +409,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     named_barrier_sync(1, kBwdThreads);  // idle warps
   }
   } else {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdComputeRegs));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(KvRegs<D>::kCompute));
     // ------------------------------------------------------------ compute warps 0-7
-    // Warp w serves TMEM lane quarter qt = w % 4 (32 rows) and column half
-    // hf = w / 4, so two warps share each scheduler and split every phase:
-    //   dS   (thread = key row): S^T / dP^T columns [64 hf, 64 hf + 64)
-    //   dQ   (thread = query row): dQ columns [hf D/2, hf D/2 + D/2)
-    //   end of unit (thread = key row): dK / dV columns [hf D/2, hf D/2 + D/2)
+    // Warp w serves TMEM lane quarter qt = w % 4 (32 key rows) and column
+    // half hf = w / 4 (64 query columns of S^T / dP^T), so two warps share
+    // each scheduler.  Per query tile, two phases, each answered by the pipe:
+    //   P:  P^T = exp2(S^T scale log2e - LSE log2e)  -> bf16 into S^T's columns
+    //   dS: dS^T = P^T (dP^T scale - D scale)        -> bf16 into dP^T's columns
+    // P stays in registers (fp32) from the first phase to the second.  At
+    // the end of a unit the dK and dV rows go out in bf16.
     const int qt = warp & 3, hf = warp >> 2;
     const int r = qt * 32 + lane;
+    const int t = threadIdx.x & 127;  // query of the tile whose LSE (warps 0-3) or D (4-7) this thread stages
     const uint32_t lane_off = static_cast<uint32_t>(qt * 32) << 16;
     float* lse2_s = reinterpret_cast<float*>(smem + L::kLse);
     float* dl_s = reinterpret_cast<float*>(smem + L::kDl);
-    long long it_global = 0;
+    // -LSE log2(e) (warps 0-3) or -D scale (warps 4-7) of query t of tile (h, i)
+    auto staged = [&](const BwdUnit& x, int it) -> float {
+      int h, i;
+      bwd_iter(p, x, it, &h, &i);
+      const int q_local = i * kTile + t;
+      if (q_local >= x.doc_len) return 0.f;
+      const long long idx = static_cast<long long>(h) * p.T + x.doc_start + q_local;
+      return threadIdx.x < 128 ? -__ldg(p.lse + idx) * 1.4426950408889634f : -__ldg(p.dl + idx) * p.scale;
+    };
+    long long g = 0;
     uint32_t units = 0;
     bool ok = true;
     for (long long k = 0; ok; ++k) {
@@ -339,97 +441,104 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (u >= total_units) break;
       const BwdUnit x = bwd_unit(p, u);
       const int key_local = x.j * kTile + r;
+      const bool key_ok = key_local < x.doc_len;
+      float pre = staged(x, 0);
       for (int it = 0; it < x.iters; ++it) {
         int h, i;
         bwd_iter(p, x, it, &h, &i);
-        // every compute warp is done with the previous tile (its LSE / D
-        // reads and its dQ staging reads), and all agree to go on
-        if (named_barrier_or(kDsBarrier, 256, !ok)) {
-          ok = false;
-          break;
-        }
-        {
-          const int t = threadIdx.x & 127;
-          const int q_local = i * kTile + t;
-          const bool qv = q_local < x.doc_len;
-          const long long tok = static_cast<long long>(x.doc_start) + q_local;
-          // stored as -LSE log2(e) and -D scale, the addends of the FMAs below
-          if (threadIdx.x < 128)
-            lse2_s[t] = qv ? -__ldg(p.lse + static_cast<long long>(h) * p.T + tok) * 1.4426950408889634f : 0.f;
-          else
-            dl_s[t] = qv ? -__ldg(p.dl + static_cast<long long>(h) * p.T + tok) * p.scale : 0.f;
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, it_global & 1, abort_word, p.err, kErrBS));
+        // S(g) done means P(g-1) of every warp was consumed (LSE free), and
+        // every warp passed the barrier of tile g-1, so finished dS(g-2)
+        // (D buffer g & 1 free)
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_word, p.err, kErrBS));
+        if (threadIdx.x < 128)
+          lse2_s[t] = pre;
+        else
+          dl_s[(g & 1) * kTile + t] = pre;
+        if (it + 1 < x.iters) pre = staged(x, it + 1);
         if (named_barrier_or(kDsBarrier, 256, !ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // ---- dS: P^T = exp2(S^T scale log2e - lse2), dS^T = P^T (dP^T - D) scale
         const int q_base = i * kTile;
-        const bool key_ok = key_local < x.doc_len;
         const int c_lo = key_local - q_base;  // query column c allowed iff c_lo <= c < c_hi
         const int c_hi = x.doc_len - q_base;
-#pragma unroll 1
+        // ---- P phase: both 32-column chunks of this half
+        uint32_t pv[2][32];
+        tmem_ld32(tS + lane_off + hf * 64, pv[0]);
+        tmem_ld32(tS + lane_off + hf * 64 + 32, pv[1]);
+        tmem_wait_ld();
+#pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = hf * 2 + cc;  // 32-column chunk of S^T / dP^T
-          uint32_t sv[32], dpv[32];
-          tmem_ld32(tS + lane_off + c * 32, sv);
-          tmem_ld32(tDP + lane_off + c * 32, dpv);
-          tmem_wait_ld();
-          uint32_t pk_p[16], pk_ds[16];
-          // P = 2^(S scale log2e - LSE log2e), dS = P (dP scale - D scale)
-          if (key_ok && c * 32 >= c_lo && c * 32 + 32 <= c_hi) {
-            // every query of the chunk is visible to this key: packed pairs
-            const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2), s2 = pack_f32x2(p.scale, p.scale);
-            const uint64_t* l2 = reinterpret_cast<const uint64_t*>(lse2_s + c * 32);
-            const uint64_t* d2 = reinterpret_cast<const uint64_t*>(dl_s + c * 32);
+          const int c0 = hf * 64 + cc * 32;
+          uint32_t pk[16];
+          if (key_ok && c0 >= c_lo && c0 + 32 <= c_hi) {
+            const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2);
+            const uint64_t* l2 = reinterpret_cast<const uint64_t*>(lse2_s + c0);
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
-              const uint64_t sp = (static_cast<uint64_t>(sv[2 * e2 + 1]) << 32) | sv[2 * e2];
-              const uint64_t dp = (static_cast<uint64_t>(dpv[2 * e2 + 1]) << 32) | dpv[2 * e2];
+              const uint64_t sp = (static_cast<uint64_t>(pv[cc][2 * e2 + 1]) << 32) | pv[cc][2 * e2];
               const uint64_t a = ffma_f32x2(sp, c2, l2[e2]);
               const float p0 = ex2_approx(lo_f32(a)), p1 = ex2_approx(hi_f32(a));
-              const uint64_t ds = fmul_f32x2(pack_f32x2(p0, p1), ffma_f32x2(dp, s2, d2[e2]));
-              pk_p[e2] = pack_bf16x2(p0, p1);
-              pk_ds[e2] = pack_bf16x2(lo_f32(ds), hi_f32(ds));
+              pv[cc][2 * e2] = __float_as_uint(p0);
+              pv[cc][2 * e2 + 1] = __float_as_uint(p1);
+              pk[e2] = pack_bf16x2(p0, p1);
             }
           } else {
-            const float4* l4 = reinterpret_cast<const float4*>(lse2_s + c * 32);
-            const float4* d4 = reinterpret_cast<const float4*>(dl_s + c * 32);
 #pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 lv = l4[e4], dv = d4[e4];
-              const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
-              float pp[4], dd[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const int e = e4 * 4 + t;
-                const int col = c * 32 + e;
-                const bool allowed = key_ok && col >= c_lo && col < c_hi;
-                const float pe = allowed ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, la[t])) : 0.f;
-                pp[t] = pe;
-                dd[t] = pe * fmaf(__uint_as_float(dpv[e]), p.scale, da[t]);
-              }
-              pk_p[e4 * 2] = pack_bf16x2(pp[0], pp[1]);
-              pk_p[e4 * 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-              pk_ds[e4 * 2] = pack_bf16x2(dd[0], dd[1]);
-              pk_ds[e4 * 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+            for (int e = 0; e < 32; ++e) {
+              const int col = c0 + e;
+              const bool allowed = key_ok && col >= c_lo && col < c_hi;
+              pv[cc][e] = __float_as_uint(
+                  allowed ? ex2_approx(fmaf(__uint_as_float(pv[cc][e]), p.scale_log2, lse2_s[col])) : 0.f);
             }
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2)
+              pk[e2] = pack_bf16x2(__uint_as_float(pv[cc][2 * e2]), __uint_as_float(pv[cc][2 * e2 + 1]));
           }
-          // P^T / dS^T (bf16 pairs) into this half's own columns, already
-          // read: half hf owns S^T / dP^T columns [64 hf, 64 hf + 64), and
-          // chunk c's pairs go to [64 hf + 16 cc, 64 hf + 16 cc + 16)
-          tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk_p);
-          tmem_st16(tDP + lane_off + hf * 64 + cc * 16, pk_ds);
+          // chunk cc's pairs go to [64 hf + 16 cc, 64 hf + 16 cc + 16): this
+          // half's own columns, already read
+          tmem_st16(tS + lane_off + hf * 64 + cc * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
-        ++it_global;
+        // ---- dS phase
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, g & 1, abort_word, p.err, kErrBS));
+        if (ok) {
+          tc_fence_after();
+          uint32_t dpv[2][32];
+          tmem_ld32(tDP + lane_off + hf * 64, dpv[0]);
+          tmem_ld32(tDP + lane_off + hf * 64 + 32, dpv[1]);
+          tmem_wait_ld();
+          const uint64_t s2 = pack_f32x2(p.scale, p.scale);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            // masked entries have P = 0 and a finite dP, so dS = 0 there
+            const uint64_t* d2 = reinterpret_cast<const uint64_t*>(dl_s + (g & 1) * kTile + hf * 64 + cc * 32);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const uint64_t pp = (static_cast<uint64_t>(pv[cc][2 * e2 + 1]) << 32) | pv[cc][2 * e2];
+              const uint64_t dp = (static_cast<uint64_t>(dpv[cc][2 * e2 + 1]) << 32) | dpv[cc][2 * e2];
+              const uint64_t dsv = fmul_f32x2(pp, ffma_f32x2(dp, s2, d2[e2]));
+              pk[e2] = pack_bf16x2(lo_f32(dsv), hi_f32(dsv));
+            }
+            tmem_st16(tDP + lane_off + hf * 64 + cc * 16, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.ds_full);
+        }
+        ++g;
       }
-      if (!ok) break;
+      // a failed dP wait in the unit's last tile is seen by every warp here
+      if (named_barrier_or(kDsBarrier, 256, !ok)) {
+        ok = false;
+        break;
+      }
       // ---- the unit's dK and dV rows (thread = key row)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkv_full, units & 1, abort_word, p.err, kErrBDkv));
       if (named_barrier_or(kDsBarrier, 256, !ok)) {
@@ -482,17 +591,18 @@ template <int D>
 struct DqSmem {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kHalfBytes = kTile * 64 * 2;
+  static constexpr int kKStages = 3;               // K(j) is read last by dQ(j), one tile later than V(j)
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
-  static constexpr int kK = kDO + kTileBytes;      // 2 stages
-  static constexpr int kV = kK + 2 * kTileBytes;   // 2 stages
+  static constexpr int kK = kDO + kTileBytes;               // 3 stages
+  static constexpr int kV = kK + kKStages * kTileBytes;     // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
   static constexpr int kBytes = kBar + 256;
 };
 
 struct DqBars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full, dp_free, p_full[2], dq_full, dq_empty, drain;
   uint32_t tmem_base;
   int abort_word;
@@ -538,9 +648,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_empty, 1);
+    for (int s = 0; s < L::kKStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_free, 8);
@@ -575,9 +689,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdControlRegs));
   if (warp == kBwdProducer) {
     // ------------------------------------------------------------ TMA producer
+    // K of key tile t (t counts the key tiles of all units of this CTA)
+    // goes to stage t % 3, V to stage t % 2.
     if (lane == 0) {
-      uint32_t units = 0, kv_uses[2] = {0, 0};
-      long long kvc = 0;
+      uint32_t units = 0, kround = 0;  // kround: completed passes over the K stages
+      int ks = 0;
+      long long kvc = 0, k_armed = 0;  // key tiles whose V / K loads were issued
       bool ok = true;
       for (long long k = 0; ok; ++k) {
         const long long u = bwd_unit_index(k, cta, nctas);
@@ -595,28 +712,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         ++units;
         for (int j = 0; j < x.ntk; ++j) {
-          const int st = static_cast<int>(kvc & 1);
-          if (kv_uses[st] > 0 &&
-              !mbar_wait(&bars.kv_empty[st], (kv_uses[st] - 1) & 1, abort_word, p.err, kErrDKvE)) {
+          const int row0 = x.doc_start + j * kTile;
+          if (kround > 0 && !mbar_wait(&bars.k_empty[ks], (kround - 1) & 1, abort_word, p.err, kErrDKvE)) {
+            k_armed = kvc;
             ok = false;
             break;
           }
-          ++kv_uses[st];
-          mbar_arrive_expect_tx(&bars.kv_full[st], 2 * L::kTileBytes);
+          mbar_arrive_expect_tx(&bars.k_full[ks], L::kTileBytes);
 #pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb) {
-            tma_load_3d(smem + L::kK + st * L::kTileBytes + hb * L::kHalfBytes, &tmK, &bars.kv_full[st], hb * 64,
-                        x.kvh, x.doc_start + j * kTile);
-            tma_load_3d(smem + L::kV + st * L::kTileBytes + hb * L::kHalfBytes, &tmV, &bars.kv_full[st], hb * 64,
-                        x.kvh, x.doc_start + j * kTile);
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem + L::kK + ks * L::kTileBytes + hb * L::kHalfBytes, &tmK, &bars.k_full[ks], hb * 64,
+                        x.kvh, row0);
+          const int vs = static_cast<int>(kvc & 1);
+          if (kvc >= 2 && !mbar_wait(&bars.v_empty[vs], ((kvc >> 1) - 1) & 1, abort_word, p.err, kErrDKvE)) {
+            k_armed = kvc + 1;
+            ok = false;
+            break;
           }
-          ++kvc;
+          mbar_arrive_expect_tx(&bars.v_full[vs], L::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem + L::kV + vs * L::kTileBytes + hb * L::kHalfBytes, &tmV, &bars.v_full[vs], hb * 64,
+                        x.kvh, row0);
+          if (++ks == L::kKStages) {
+            ks = 0;
+            ++kround;
+          }
+          k_armed = ++kvc;
         }
       }
       if (!ok) {
+        // every armed barrier completes once its bytes land
         if (units > 0) bwd_drain_wait(&bars.q_full, (units - 1) & 1);
-        for (int s = 0; s < 2; ++s)
-          if (kv_uses[s] > 0) bwd_drain_wait(&bars.kv_full[s], (kv_uses[s] - 1) & 1);
+        for (int s = 0; s < L::kKStages; ++s) {
+          const long long uses = (k_armed + L::kKStages - 1 - s) / L::kKStages;
+          if (uses > 0) bwd_drain_wait(&bars.k_full[s], static_cast<uint32_t>(uses - 1) & 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+          const long long uses = (kvc + 1 - s) / 2;
+          if (uses > 0) bwd_drain_wait(&bars.v_full[s], static_cast<uint32_t>(uses - 1) & 1);
+        }
       }
     }
     __syncwarp();
@@ -633,23 +768,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
       const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
       const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), L::kHalfBytes, 1024);
-      uint32_t units = 0;
-      long long kvc = 0;  // key tiles issued so far (all units): stage, S buffer and barrier phases
+      uint32_t units = 0, kround = 0;
+      int ks = 0, ks_prev = 0;  // K stages of this key tile and of the previous one
+      long long kvc = 0;  // key tiles issued so far (all units): stages, S buffer and barrier phases
       bool ok = true;
-      // dQ += dS(t) K(t) for global tile t (its dS sits in S buffer t & 1, its K in stage t & 1)
-      auto issue_dq = [&](long long t, bool first_of_unit) -> bool {
+      // dQ += dS(t) K(t) for global tile t (its dS sits in S buffer t & 1, its K in stage kst)
+      auto issue_dq = [&](long long t, int kst, bool first_of_unit) -> bool {
         if (!mbar_wait(&bars.p_full[t & 1], (t >> 1) & 1, abort_word, p.err, kErrDP)) return false;
         if (first_of_unit && units > 0 &&
             !mbar_wait(&bars.dq_empty, (units - 1) & 1, abort_word, p.err, kErrDDqE))
           return false;
         tc_fence_after();
         const uint32_t a = tS0 + static_cast<uint32_t>(t & 1) * 128u;
-        const uint64_t b = dK_mn + static_cast<uint64_t>(t & 1) * kTileUnits;
+        const uint64_t b = dK_mn + static_cast<uint64_t>(kst) * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(tDQ, a + kk * 8 + (kk >= 4 ? 32 : 0), b + (static_cast<uint64_t>(kk * 2048) >> 4), idesc_q,
                   (first_of_unit && kk == 0) ? 0u : 1u);
-        umma_commit(&bars.kv_empty[t & 1]);
+        umma_commit(&bars.k_empty[kst]);
         return true;
       };
       for (long long k = 0; ok; ++k) {
@@ -660,13 +796,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         for (int j = 0; j < x.ntk && ok; ++j) {
           const int st = static_cast<int>(kvc & 1);
-          ok = mbar_wait(&bars.kv_full[st], (kvc >> 1) & 1, abort_word, p.err, kErrDKv);
+          ok = mbar_wait(&bars.k_full[ks], kround & 1, abort_word, p.err, kErrDKv);
           if (!ok) break;
           // S(j) into buffer st: its previous dS was read by a dQ MMA issued earlier
+          const uint64_t kd = dK_k + static_cast<uint64_t>(ks) * kTileUnits;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
-            umma_ss(tS0 + st * 128u, dQ_k + off, dK_k + st * kTileUnits + off, idesc_s, kk > 0);
+            umma_ss(tS0 + st * 128u, dQ_k + off, kd + off, idesc_s, kk > 0);
           }
           // dP(j) once the compute warps have read dP(j-1)
           if (kvc > 0) {
@@ -674,18 +811,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
+          ok = mbar_wait(&bars.v_full[st], (kvc >> 1) & 1, abort_word, p.err, kErrDKv);
+          if (!ok) break;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
             umma_ss(tDP, dDO_k + off, dV_k + st * kTileUnits + off, idesc_s, kk > 0);
           }
+          umma_commit(&bars.v_empty[st]);  // V(j) is read by dP(j) alone
           umma_commit(&bars.s_full);
           if (j == x.ntk - 1) umma_commit(&bars.q_empty);  // Q and dO are read by then
           // dQ of the previous tile of this unit
-          if (j > 0) ok = issue_dq(kvc - 1, j == 1);
+          if (j > 0) ok = issue_dq(kvc - 1, ks_prev, j == 1);
+          ks_prev = ks;
+          if (++ks == L::kKStages) {
+            ks = 0;
+            ++kround;
+          }
           ++kvc;
         }
-        if (ok) ok = issue_dq(kvc - 1, x.ntk == 1);
+        if (ok) ok = issue_dq(kvc - 1, ks_prev, x.ntk == 1);
         if (ok) umma_commit(&bars.dq_full);
         ++units;
       }
