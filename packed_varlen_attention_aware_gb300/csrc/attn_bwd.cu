@@ -125,17 +125,11 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, long long u) {
   return x;
 }
 
-// Iteration k of a unit: query head and query tile.  Query tiles run from
-// the document's last tile down to the key tile's diagonal, so every unit of
-// a document starts at the same tile: the CTAs working on one GQA group read
-// the same Q / dO tiles and add into the same dQ rows at about the same time,
+// The iterations of a unit: for each query head of the GQA group in turn,
+// the query tiles from the document's last one down to the key tile's
+// diagonal.  Every unit of a document starts at the same tile, so the CTAs
+// working on one GQA group read the same Q / dO tiles at about the same time
 // and those stay in L2.
-__device__ __forceinline__ void bwd_iter(const BwdParams& p, const BwdUnit& x, int k, int* h, int* i) {
-  const int per = x.n - x.j;
-  *h = x.kvh * p.group + k / per;
-  *i = x.n - 1 - k % per;
-}
-
 __device__ __forceinline__ long long bwd_unit_index(long long k, int cta, int nctas) {
   return k * nctas + ((k & 1) ? (nctas - 1 - cta) : cta);
 }
@@ -226,9 +220,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(smem + L::kV + hb * L::kHalfBytes, &tmV, &bars.kv_full, hb * 64, x.kvh, x.k_row0);
         }
         ++units;
+        int h = x.kvh * p.group, i = x.n - 1;  // query head and tile of iteration it
         for (int it = 0; it < x.iters; ++it) {
-          int h, i;
-          bwd_iter(p, x, it, &h, &i);
           const int q_row0 = x.doc_start + i * kTile;
           if (qround > 0 && !mbar_wait(&bars.q_empty[qs], (qround - 1) & 1, abort_word, p.err, kErrBQE)) {
             q_armed = g;
@@ -256,6 +249,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ++qround;
           }
           q_armed = ++g;
+          if (i == x.j) {
+            i = x.n - 1;
+            ++h;
+          } else {
+            --i;
+          }
         }
       }
       if (!ok) {
@@ -424,14 +423,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(qt * 32) << 16;
     float* lse2_s = reinterpret_cast<float*>(smem + L::kLse);
     float* dl_s = reinterpret_cast<float*>(smem + L::kDl);
-    // -LSE log2(e) (warps 0-3) or -D scale (warps 4-7) of query t of tile (h, i)
-    auto staged = [&](const BwdUnit& x, int it) -> float {
-      int h, i;
-      bwd_iter(p, x, it, &h, &i);
+    // LSE (warps 0-3) or D (warps 4-7) of query t of tile (h, i), 0 past the
+    // document's end.  Nothing here uses the loaded value, so the load stays
+    // in flight until the value is staged one tile later.
+    const float* src = threadIdx.x < 128 ? p.lse : p.dl;
+    const float mult = threadIdx.x < 128 ? -1.4426950408889634f : -p.scale;
+    auto staged = [&](const BwdUnit& x, int h, int i) -> float {
       const int q_local = i * kTile + t;
-      if (q_local >= x.doc_len) return 0.f;
-      const long long idx = static_cast<long long>(h) * p.T + x.doc_start + q_local;
-      return threadIdx.x < 128 ? -__ldg(p.lse + idx) * 1.4426950408889634f : -__ldg(p.dl + idx) * p.scale;
+      float v = 0.f;
+      if (q_local < x.doc_len) v = ldg_f32_here(src + static_cast<long long>(h) * p.T + x.doc_start + q_local);
+      return v;
     };
     long long g = 0;
     uint32_t units = 0;
@@ -442,19 +443,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdUnit x = bwd_unit(p, u);
       const int key_local = x.j * kTile + r;
       const bool key_ok = key_local < x.doc_len;
-      float pre = staged(x, 0);
+      // query tile i from n - 1 down to j, then the next head of the group
+      int i = x.n - 1;                               // this iteration's query tile
+      int nh = x.kvh * p.group, ni = x.n - 1;        // the tile `pre` is loaded for
+      float pre = staged(x, nh, ni);
       for (int it = 0; it < x.iters; ++it) {
-        int h, i;
-        bwd_iter(p, x, it, &h, &i);
         // S(g) done means P(g-1) of every warp was consumed (LSE free), and
         // every warp passed the barrier of tile g-1, so finished dS(g-2)
         // (D buffer g & 1 free)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_word, p.err, kErrBS));
+        // stored as -LSE log2(e) and -D scale, the addends of the FMAs below
         if (threadIdx.x < 128)
-          lse2_s[t] = pre;
+          lse2_s[t] = pre * mult;
         else
-          dl_s[(g & 1) * kTile + t] = pre;
-        if (it + 1 < x.iters) pre = staged(x, it + 1);
+          dl_s[(g & 1) * kTile + t] = pre * mult;
         if (named_barrier_or(kDsBarrier, 256, !ok)) {
           ok = false;
           break;
@@ -504,6 +506,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
+        // the next tile's LSE / D: it has a whole tile to land
+        if (ni == x.j) {
+          ni = x.n - 1;
+          ++nh;
+        } else {
+          --ni;
+        }
+        if (it + 1 < x.iters) pre = staged(x, nh, ni);
         // ---- dS phase
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, g & 1, abort_word, p.err, kErrBS));
         if (ok) {
@@ -532,6 +542,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.ds_full);
         }
+        i = i == x.j ? x.n - 1 : i - 1;
         ++g;
       }
       // a failed dP wait in the unit's last tile is seen by every warp here
