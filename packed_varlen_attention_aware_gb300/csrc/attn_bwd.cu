@@ -476,11 +476,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pk[16];
           if (key_ok && c0 >= c_lo && c0 + 32 <= c_hi) {
             const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2);
-            const uint64_t* l2 = reinterpret_cast<const uint64_t*>(lse2_s + c0);
+            const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(lse2_s + c0);
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
+              const ulonglong2 lv = l4[e2 >> 1];
               const uint64_t sp = (static_cast<uint64_t>(pv[cc][2 * e2 + 1]) << 32) | pv[cc][2 * e2];
-              const uint64_t a = ffma_f32x2(sp, c2, l2[e2]);
+              const uint64_t a = ffma_f32x2(sp, c2, (e2 & 1) ? lv.y : lv.x);
               const float p0 = ex2_approx(lo_f32(a)), p1 = ex2_approx(hi_f32(a));
               pv[cc][2 * e2] = __float_as_uint(p0);
               pv[cc][2 * e2 + 1] = __float_as_uint(p1);
@@ -526,13 +527,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             // masked entries have P = 0 and a finite dP, so dS = 0 there
-            const uint64_t* d2 = reinterpret_cast<const uint64_t*>(dl_s + (g & 1) * kTile + hf * 64 + cc * 32);
+            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(dl_s + (g & 1) * kTile + hf * 64 + cc * 32);
             uint32_t pk[16];
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
+              const ulonglong2 dv = d4[e2 >> 1];
               const uint64_t pp = (static_cast<uint64_t>(pv[cc][2 * e2 + 1]) << 32) | pv[cc][2 * e2];
               const uint64_t dp = (static_cast<uint64_t>(dpv[cc][2 * e2 + 1]) << 32) | dpv[cc][2 * e2];
-              const uint64_t dsv = fmul_f32x2(pp, ffma_f32x2(dp, s2, d2[e2]));
+              const uint64_t dsv = fmul_f32x2(pp, ffma_f32x2(dp, s2, (e2 & 1) ? dv.y : dv.x));
               pk[e2] = pack_bf16x2(lo_f32(dsv), hi_f32(dsv));
             }
             tmem_st16(tDP + lane_off + hf * 64 + cc * 16, pk);
