@@ -48,6 +48,15 @@ hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, i
 
 namespace {
 
+// Read-only global load that the compiler keeps where it is written (an
+// ordinary __ldg may be sunk to its first use, past barriers, and then its
+// whole latency is paid there).
+__device__ __forceinline__ float ldg_f32_here(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 constexpr int kBwdThreads = 384;
 constexpr int kBwdProducer = 8;
 constexpr int kBwdMma = 9;

@@ -259,14 +259,6 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bo
       : "memory");
   return r != 0;
 }
-// Read-only global load that the compiler keeps where it is written (an
-// ordinary __ldg may be sunk to its first use, past barriers, and then its
-// whole latency is paid there).
-__device__ __forceinline__ float ldg_f32_here(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
