@@ -30,7 +30,10 @@
 //   dV  += P^T dO_i       dK  += dS^T Q_i             (TS, A from TMEM)
 // TMEM (512 columns): dV [0,D) dK [D,2D) S^T [2D,2D+128) dP^T [2D+128,2D+256);
 // P^T aliases S^T's columns [0,32) and [64,96) (one block per column half),
-// dS^T the same columns of dP^T.
+// dS^T the same columns of dP^T.  The compute warps hand P^T and dS^T back
+// separately, and the products are issued as
+//   S(i) dP(i) | dV(i) S(i+1) | dK(i) dP(i+1) | dV(i+1) S(i+2) | ...
+// so the tensor pipe runs two products while the warps compute each phase.
 // Every wait is bounded; a timeout sets the device error word and all roles
 // stop at the same point, drain and free TMEM.
 #include <cuda.h>
@@ -1000,6 +1003,12 @@ __global__ void k_bwd_delta(const __nv_bfloat16* __restrict__ o, const __nv_bflo
     dl[static_cast<long long>(h) * T + t] = acc;
   }
 }
+
+// dynamic shared memory of a launch = layout + 1 KB for the 1024-byte
+// alignment of the swizzled tiles; the per-block opt-in limit is 227 KB
+static_assert(BwdSmem<128>::kBytes + 1024 <= 227 * 1024, "dK/dV pass shared memory");
+static_assert(DqSmem<128>::kBytes + 1024 <= 227 * 1024, "dQ pass shared memory");
+static_assert(sizeof(BwdBars) <= 256 && sizeof(DqBars) <= 256, "barrier block");
 
 size_t bwd_align256(size_t x) { return (x + 255) & ~size_t(255); }
 
