@@ -90,8 +90,8 @@ struct BwdSmem {
   static constexpr int kQ = kV + kTileBytes;                    // 3 stages
   static constexpr int kDO = kQ + kQStages * kTileBytes;        // 2 stages
   static constexpr int kLse = kDO + 2 * kTileBytes;  // 128 fp32: -LSE log2(e) of the tile's queries
-  static constexpr int kDl = kLse + kTile * 4;       // 2 x 128 fp32: -D scale, by tile parity
-  static constexpr int kBar = kDl + 2 * kTile * 4;
+  static constexpr int kDl = kLse + kTile * 4;       // 128 fp32: -D scale of the tile's queries
+  static constexpr int kBar = kDl + kTile * 4;
   static constexpr int kBytes = kBar + 256;
 };
 
@@ -458,27 +458,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // query tile i from n - 1 down to j, then the next head of the group
       int i = x.n - 1;                               // this iteration's query tile
       int nh = x.kvh * p.group, ni = x.n - 1;        // the tile `pre` is loaded for
+      // Staging: -LSE log2(e) and -D scale (the addends of the FMAs below)
+      // of a tile's queries are written once every warp is done with the
+      // previous tile, behind the dS phase, where the warps wait for the next
+      // S anyway.  The unit's first tile: every warp passed the previous
+      // unit's last barrier.
       float pre = staged(x, nh, ni);
+      if (threadIdx.x < 128)
+        lse2_s[t] = pre * mult;
+      else
+        dl_s[t] = pre * mult;
+      if (named_barrier_or(kDsBarrier, 256, !ok)) {
+        ok = false;
+        break;
+      }
       for (int it = 0; it < x.iters; ++it) {
-        // S(g) done means P(g-1) of every warp was consumed (LSE free), and
-        // every warp passed the barrier of tile g-1, so finished dS(g-2)
-        // (D buffer g & 1 free)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_word, p.err, kErrBS));
-        // stored as -LSE log2(e) and -D scale, the addends of the FMAs below
-        if (threadIdx.x < 128)
-          lse2_s[t] = pre * mult;
-        else
-          dl_s[(g & 1) * kTile + t] = pre * mult;
-        if (named_barrier_or(kDsBarrier, 256, !ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         const int q_base = i * kTile;
         const int c_lo = key_local - q_base;  // query column c allowed iff c_lo <= c < c_hi
         const int c_hi = x.doc_len - q_base;
-        // ---- P phase: both 32-column chunks of this half
+        // ---- P phase: both 32-column chunks of this half (after a failed
+        // wait it runs on stale columns; every role is stopping by then)
         uint32_t pv[2][32];
+        tc_fence_after();
         tmem_ld32(tS + lane_off + hf * 64, pv[0]);
         tmem_ld32(tS + lane_off + hf * 64 + 32, pv[1]);
         tmem_wait_ld();
@@ -539,7 +541,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             // masked entries have P = 0 and a finite dP, so dS = 0 there
-            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(dl_s + (g & 1) * kTile + hf * 64 + cc * 32);
+            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(dl_s + hf * 64 + cc * 32);
             uint32_t pk[16];
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
@@ -555,6 +557,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.ds_full);
+        }
+        if (it + 1 < x.iters) {
+          // every warp is done with this tile's LSE / D: stage the next
+          // tile's, and make them visible before its P phase
+          if (named_barrier_or(kDsBarrier, 256, !ok)) {
+            ok = false;
+            break;
+          }
+          if (threadIdx.x < 128)
+            lse2_s[t] = pre * mult;
+          else
+            dl_s[t] = pre * mult;
+          named_barrier_or(kDsBarrier, 256, false);
         }
         i = i == x.j ? x.n - 1 : i - 1;
         ++g;
