@@ -665,7 +665,7 @@ def backward_mode(args):
     out = {"mode": "backward", "workload": workload_config(w, args, "fused")["workload"], "steps": args.steps, "warmup": args.warmup,
            "fwd_ms": fm, "bwd_ms": bm, "fwd_tflops": flops_fwd / (fm * 1e-3) / 1e12, "bwd_tflops": bw,
            "step_tflops": (flops_fwd + flops_bwd) / ((fm + bm) * 1e-3) / 1e12,
-           "roofline": {"bound": "tensor", "kernel": "k_attn_bwd (+ delta and dq conversion)", "achieved": bw,
+           "roofline": {"bound": "tensor", "kernel": "whole backward: k_bwd_delta, k_attn_bwd (dK, dV), k_attn_bwd_dq (dQ)", "achieved": bw,
                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": bw / peaks["bf16_tflops"],
                         "peak_source": src},
            "clocks": clocks.summary()}
