@@ -10,11 +10,17 @@ One step = the whole hot path on one micro-batch resident in HBM:
 Metric: useful causal-attention TFLOP/s, 4*d*Hq*sum_i s_i(s_i+1)/2 per step,
 and its fraction of the bf16 dense tensor peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mb32k]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload seq2m]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
-Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
-independent replica (weak scaling, no data-path collective).
+The default workload is the largest single-GPU one: one 2,097,152-token
+sequence, C = 8,192 (256 chunks, 32,896 causal blocks), Hq = 32, Hkv = 8,
+d = 128.  After it, the 131,072-token sequence is timed in FUSED and SPLIT
+mode as extra entries of the same line.
+
+Prints ONE JSON line (rank 0).  With --gpus N > 1 the script starts N ranks
+itself (torchrun, one per GPU) unless it already runs under torchrun; every
+rank runs an independent replica (weak scaling, no data-path collective).
 """
 from __future__ import annotations
 
@@ -37,7 +43,6 @@ sys.path.insert(0, ROOT)
 METRIC = "varlen causal attention fwd useful TFLOP/s and fraction of GB300 BF16 peak"
 L2_BYTES = 129 * 10**6
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_mb32k.md")
 ATTN_SRC = os.path.join(ROOT, "packed_varlen_attention_aware_gb300", "csrc", "attn_fwd.cu")
 
 
@@ -71,19 +76,11 @@ def attn_kernel_source_sha256() -> str:
     return hashlib.sha256((src[:cut] + ptx).encode()).hexdigest()
 
 
-def traffic_from_profile():
-    """dram bytes per attention launch from the committed ncu summary, valid
-    only while the kernel source is the one that was profiled."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
-    want = attn_kernel_source_sha256()
-    sha, dram = None, None
-    for line in open(TRAFFIC_FILE):
-        if line.startswith("kernel_source_sha256:"):
-            sha = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            dram = float(line.split(":", 1)[1].strip())
-    return dram if sha == want else None
+# DRAM bytes per attention launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# from the ncu captures summarised under profiles/, keyed by (workload, mode).
+# A figure is reported only while the attention kernel's device source hashes
+# to the value it was captured with.
+PROFILED_TRAFFIC = {}
 
 
 class ClockSampler:
@@ -220,8 +217,11 @@ def reference_arm(args, rank):
     from packed_varlen_attention_aware_gb300 import workloads as wl
 
     w = wl.workload(args.workload, args.seed)
-    q, k, v = wl.qkv(w, device="cpu")
-    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    # the same seeded bytes as our arm: large workloads are drawn by the GPU's
+    # generator (input generation only; the timed work is the CPU oracle)
+    big = w.total_tokens > (1 << 17)
+    q, k, v = wl.qkv(w, device="cuda" if big and torch.cuda.is_available() else "cpu")
+    per_step = args.ref_step_seconds or max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, per_step, args.seed + 1000)
     flops, secs, rows = 0, 0.0, 0
@@ -260,6 +260,117 @@ def workload_config(w, args, mode):
 
 # ---------------------------------------------------------------- our arm
 
+def gpu_numa_node(dev_index: int):
+    """The host NUMA node nearest the GPU (its PCI device's numa_node), or None."""
+    import torch
+
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        bdf = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        node = int(open(f"/sys/bus/pci/devices/{bdf}/numa_node").read().strip())
+        return node if node >= 0 else None
+    except Exception:
+        return None
+
+
+def bind_to_numa_node(node):
+    """Run this process on the CPUs of `node`, so pinned host buffers it
+    allocates afterwards are placed (first touch) in that node's memory.
+    Returns the CPU count bound to, or None when nothing was changed."""
+    if node is None:
+        return None
+    try:
+        cpus = set()
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return len(cpus)
+    except Exception:
+        return None
+
+
+def shard_report(shard_flops, nshards: int):
+    """Per-shard useful FLOPs of the step (hdp_flops_per_shard) and their
+    max/mean imbalance."""
+    f = [int(x) for x in shard_flops[:nshards].cpu().tolist()]
+    mean = sum(f) / max(1, len(f))
+    out = {"num_shards": nshards, "max": max(f), "mean": mean, "max_over_mean": max(f) / mean if mean else None}
+    if nshards <= 512:
+        out["flops"] = f
+    return out
+
+
+def flops_spread(name: str, seeds, dev):
+    """Useful FLOPs of the workload's micro-batch for each seed, from the
+    library's per-shard FLOPs (the lengths differ by seed)."""
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    per_seed = []
+    for sd in seeds:
+        w = wl.workload(name, sd)
+        dl = torch.tensor(w.lengths, dtype=torch.int32, device=dev)
+        with pkg.hdp_plan_create(dl, w.capacity) as plan:
+            f = torch.empty(plan.view.num_shards, dtype=torch.int64, device=dev)
+            pkg.hdp_flops_per_shard(plan, w.d, w.hq, f)
+            per_seed.append(int(f.sum().item()))
+    return {"seeds": list(seeds), "useful_flops": per_seed, "min": min(per_seed), "max": max(per_seed),
+            "max_over_min": max(per_seed) / min(per_seed)}
+
+
+def attention_only(name: str, mode_name: str, seed: int, warmup: int, steps: int, dev, peaks):
+    """CUDA-event time of the attention call alone (plan made once) on another
+    named workload, for the extra timed entries of the line."""
+    import torch
+
+    import packed_varlen_attention_aware_gb300 as pkg
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    w = wl.workload(name, seed)
+    mode = pkg.HDP_MODE_SPLIT if mode_name == "split" else pkg.HDP_MODE_FUSED
+    q, k, v = wl.qkv(w, device=str(dev))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, w.total_tokens), dtype=torch.float32, device=dev)
+    dl = torch.tensor(w.lengths, dtype=torch.int32, device=dev)
+    plan = pkg.hdp_plan_create(dl, w.capacity)
+    wsb = pkg.hdp_attention_workspace_bytes(plan, w.hq, w.d, mode)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+    stream = torch.cuda.current_stream()
+    times = []
+    with ClockSampler(dev.index or 0) as clocks:
+        for it in range(warmup + steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, mode, ws, o, lse, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= warmup:
+                times.append(e0.elapsed_time(e1))
+    pkg.hdp_device_status()
+    plan.destroy()
+    flops = useful_flops(w.lengths, w.d, w.hq)
+    ms = statistics.mean(times)
+    achieved = flops / (ms * 1e-3) / 1e12
+    out = {"workload": workload_config(w, None, mode_name)["workload"], "mode": mode_name, "warmup": warmup,
+           "steps": steps, "attn_ms": ms, "attn_ms_min": min(times), "achieved": achieved, "unit": "TFLOP/s",
+           "frac": achieved / peaks["bf16_tflops"], "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+           "kernel": "k_attn_fwd" + (" + k_merge_blocks" if mode_name == "split" else ""),
+           "clocks": clocks.summary()}
+    prof = PROFILED_TRAFFIC.get((name, mode_name))
+    if prof and prof["kernel_source_sha256"] == attn_kernel_source_sha256():
+        out["traffic"] = prof["dram_bytes_per_launch"]
+        out["traffic_source"] = prof["source"]
+    del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def our_arm(args, ws, rank, local):
     import torch
     import torch.distributed as dist
@@ -271,6 +382,8 @@ def our_arm(args, ws, rank, local):
     native_build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    numa_node = gpu_numa_node(local)
+    numa_cpus = bind_to_numa_node(numa_node)
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = wl.workload(args.workload, args.seed + rank)
@@ -332,16 +445,26 @@ def our_arm(args, ws, rank, local):
     ms = t0.elapsed_time(t1)
     attn_ms = sum(a.elapsed_time(b) for a, b in attn_events) / len(attn_events)
     clk = clocks.summary()
+    shards = shard_report(shard_flops, nshards)
 
     # ---- end to end through the public API with host buffers.  Every step
     # copies its inputs from pinned host memory, runs the path and reads its
     # outputs back; step i+1's upload and step i-1's download run on their own
-    # streams while step i computes (two device buffer sets).
-    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    # streams while step i computes (two device buffer sets).  Steps of more
+    # than a second (the 2M-token sequence) run this leg over fewer steps.
+    long_step = ms / args.steps > 1000.0
+    e2e_steps = min(args.steps, 3) if long_step else args.steps
+    e2e_warm = 1 if long_step else max(2, args.warmup // 2)
+
+    def pinned_like(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+    qh, kh, vh = pinned_like(q), pinned_like(k), pinned_like(v)
+    qh.copy_(q)
+    kh.copy_(k)
+    vh.copy_(v)
     lh = torch.tensor(w.lengths, dtype=torch.int32).pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    fh = torch.empty(shard_flops.shape, dtype=torch.int64).pin_memory()
+    oh, lseh, fh = pinned_like(o), pinned_like(lse), pinned_like(shard_flops)
     qd = [q, torch.empty_like(q)]
     kd = [k, torch.empty_like(k)]
     vd = [v, torch.empty_like(v)]
@@ -353,7 +476,6 @@ def our_arm(args, ws, rank, local):
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_done = [torch.cuda.Event(), torch.cuda.Event()]
     ev_out = [torch.cuda.Event(), torch.cuda.Event()]
-
     def upload(i):
         b = i & 1
         with torch.cuda.stream(s_in):
@@ -389,51 +511,95 @@ def our_arm(args, ws, rank, local):
 
     for b in range(2):
         ev_out[b].record(s_out)
-    e2e_run(max(2, args.warmup // 2))
+    e2e_run(e2e_warm)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     s_in.wait_stream(stream)
-    e2e_run(args.steps)
+    e2e_run(e2e_steps)
     stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    pkg.hdp_device_status()
     h2d = in_bytes + lh.numel() * 4
     d2h = oh.numel() * 2 + lseh.numel() * 4 + fh.numel() * 8
+    # the host link alone, per direction: one step's uploads, then its downloads
+    rates = {}
+    for direction in ("h2d", "d2h"):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(s_in)
+        with torch.cuda.stream(s_in):
+            if direction == "h2d":
+                qd[1].copy_(qh, non_blocking=True)
+                kd[1].copy_(kh, non_blocking=True)
+                vd[1].copy_(vh, non_blocking=True)
+            else:
+                oh.copy_(od[1], non_blocking=True)
+                lseh.copy_(lsed[1], non_blocking=True)
+        c1.record(s_in)
+        torch.cuda.synchronize()
+        nbytes = in_bytes if direction == "h2d" else oh.numel() * 2 + lseh.numel() * 4
+        rates[direction] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    del qh, kh, vh, oh, lseh, qd, kd, vd, od, lsed
 
     (ms, e2e_ms, attn_ms_max), job_flops = aggregate_over_ranks([ms, e2e_ms, attn_ms], flops_step, ws, dev)
 
+    peaks, src = load_peaks()
+    extras = {}
+    if rank == 0 and ws == 1 and not args.no_extras:
+        del o, lse, workspace
+        if args.workload == "seq2m":
+            q = k = v = None  # room for the 128K workload's SPLIT partials
+        torch.cuda.empty_cache()
+        if args.workload == "seq2m":
+            for m in ("fused", "split"):
+                extras[f"seq128k_{m}"] = attention_only("seq128k", m, args.seed, 3, 10, dev, peaks)
+        if args.workload == "mb32k":
+            extras["mb32k_useful_flops_by_seed"] = flops_spread("mb32k", range(10), dev)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        if q is None:
+            q, k, v = wl.qkv(w, device=str(dev))
         f, secs, rows, threads = oracle_sample(w, q, k, v, args.cpu_seconds, args.seed + 7)
         cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} random (token, head) rows of {w.name}, {secs:.1f} s, fp64 C oracle with "
                          f"OpenMP on {cpu_model()}"}
     if rank == 0:
-        peaks, src = load_peaks()
         achieved = flops_step / (attn_ms * 1e-3) / 1e12
         value = job_throughput(job_flops, args.steps, ms)
+        prof = PROFILED_TRAFFIC.get((args.workload, args.mode))
+        traffic = None
+        if prof and prof["kernel_source_sha256"] == attn_kernel_source_sha256():
+            traffic = prof["dram_bytes_per_launch"]
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, args, args.mode),
+            "config": dict(workload_config(w, args, args.mode), shards=shards),
             "frac_of_bf16_peak": value / (peaks["bf16_tflops"] * ws),
             "roofline": {"bound": "tensor", "kernel": "k_attn_fwd", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "peak_source": f"{src} bf16 dense burst",
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "attn_ms": attn_ms, "traffic": traffic_from_profile()},
+                         "attn_ms": attn_ms, "traffic": traffic,
+                         "traffic_note": None if traffic is not None else
+                         "no ncu capture of this kernel on this workload fits the capture size rule; "
+                         "see the seq128k entries"},
             "cpu_baseline": cpu,
-            "e2e": {"value": job_throughput(job_flops, args.steps, e2e_ms), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
-                    "pipeline": "step i+1 upload and step i-1 download overlap step i compute"},
+            "e2e": {"value": job_throughput(job_flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
+                    "steps": e2e_steps, "warmup": e2e_warm,
+                    "pipeline": "step i+1 upload and step i-1 download overlap step i compute",
+                    "copy_gbs": rates, "numa_node": numa_node, "numa_cpus_bound": numa_cpus},
             "gpu_launches": launches,
             "clocks": clk,
         }
+        if extras:
+            line["extra"] = extras
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -673,17 +839,37 @@ def backward_mode(args):
     return 0
 
 
-def main():
+def free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launcher_command(argv, gpus: int, port: int):
+    """torchrun command that runs this script with the same arguments as
+    `gpus` ranks on this node (one process per GPU)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mb32k", choices=["tiny", "mb32k", "seq128k", "mix1m", "seq2m"])
+    ap.add_argument("--workload", default="seq2m", choices=["tiny", "mb32k", "seq128k", "mix1m", "seq2m"])
     ap.add_argument("--mode", choices=["fused", "split"], default="fused")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the extra entries (128K FUSED/SPLIT after seq2m, the FLOP spread of mb32k)")
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: CPU seconds per step (default: about 150 s over all steps)")
     ap.add_argument("--kernels", action="store_true", help="time the plan stress input and the LSE merge")
     ap.add_argument("--cost-model", action="store_true",
                     help="calibrate T(s) and t_blk on this GPU and apply the ring model")
@@ -691,10 +877,17 @@ def main():
                     help="balance scheduler on the per-shard FLOPs of the 1M-token mixture")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (after the forward) on --workload")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: start the ranks here
+        return subprocess.call(launcher_command(argv, args.gpus, free_port()))
     ws, rank, local = dist_setup()
+    if ws != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {ws}")
     if args.kernels:
         return kernels_mode(args) if rank == 0 else 0
     if args.cost_model:

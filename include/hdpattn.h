@@ -113,7 +113,8 @@ typedef struct {
  *   num_docs   >= 1.      capacity >= 1.
  *   flags      HDP_PLAN_DEFAULT or HDP_PLAN_NO_SHARDS.
  *   out        receives the plan (NULL on failure).
- * Blocks the host once to read the totals.  Fails with INVALID_ARGUMENT for a
+ * Blocks the host once, to read the totals and the shard count back (best fit
+ * runs on the device before that read-back).  Fails with INVALID_ARGUMENT for a
  * length < 1 or T >= 2^31, UNSUPPORTED when more than 65,536 sub-capacity
  * pieces need best-fit packing (use HDP_PLAN_NO_SHARDS), OUT_OF_MEMORY if the
  * tables cannot be allocated.  Tables are allocated stream-ordered on
@@ -158,22 +159,27 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
 /*
  * SPLIT-mode attention that allocates nothing.  The paper has no counterpart;
  * this entry exists for callers that cannot allocate device memory at the time
- * they run attention: code running while a CUDA graph is being captured
- * (cudaMalloc cannot be captured), servers that reserve all device memory up
- * front and forbid allocation on the request path, and callers that must avoid
- * the device-wide synchronisation cudaMalloc/cudaFree can imply.
+ * they run attention: serving processes that reserve all device memory at
+ * start-up and forbid allocation on the request path, host programs whose own
+ * allocator owns the device memory, and callers that must avoid the
+ * device-wide synchronisation cudaMalloc/cudaFree can imply.
  * Same arguments and results as hdp_attention_fwd with mode HDP_MODE_SPLIT,
- * but the partials live in a fixed 64 MiB scratch area inside the library
- * (every GPU that loads the library reserves it until the process exits).
+ * but the partials live in a fixed 64 MiB scratch array inside the library
+ * (every GPU that loads the library holds it until the process exits).
  *   - Plans whose SPLIT workspace (hdp_attention_workspace_bytes) exceeds
  *     64 MiB are rejected with HDP_ERR_INVALID_ARGUMENT and a message.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
- *     call on a device resolves the scratch area's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
- *   - Every call shares the one scratch area and overwrites it; nothing in it
- *     needs to start at zero.  Calls that overlap on the GPU (other streams,
- *     other threads) race on it and must be serialised by the caller.
+ *     call on a device resolves the scratch array's device address (once per
+ *     device, with that device current) and caches it; make that first call
+ *     before any stream capture.  A cudaDeviceReset, or anything else that
+ *     destroys the device's primary context, invalidates the cached address
+ *     (and the device error word's): do not call the library on that device
+ *     after such a reset in the same process.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents; every partial a call reads is written by that call first, so
+ *     nothing needs to start at zero.  Calls that overlap on the GPU (other
+ *     streams, other threads) race on the array and must be serialised by the
+ *     caller.
  */
 hdp_status_t hdp_attention_fwd_split_noalloc(hdp_plan_t plan, const void* q, const void* k, const void* v,
                                              int32_t hq, int32_t hkv, int32_t d, float scale, void* o, float* lse,
@@ -243,6 +249,25 @@ const char* hdp_last_error_message(void);
 /* Number of CUDA kernels this library has enqueued in this process (all
  * devices, all threads).  Diagnostic counter; never reset. */
 uint64_t hdp_kernel_launch_count(void);
+
+/* Number of times this library has blocked the host on a stream in this
+ * process: hdp_plan_create's one read-back and hdp_device_status.  Diagnostic
+ * counter; never reset. */
+uint64_t hdp_host_sync_count(void);
+
+/*
+ * Budget of the attention forward's bounded waits, in SM clocks, for the
+ * launches this process makes after the call (all devices, all threads).
+ * clocks <= 0 restores the default of 2e9 clocks (about one second at
+ * 2 GHz); no legitimate wait lasts more than a few microseconds.  A budget of
+ * a few clocks makes the first wait that is not already satisfied expire: the
+ * kernel then records the expiry, stops every role, waits (on its own,
+ * unchanged budget) for the copies and tensor-core work it has in flight,
+ * frees its tensor memory and returns, and hdp_device_status reports
+ * HDP_ERR_DEVICE_TIMEOUT.  This is how the timeout path is tested without a
+ * fault; production code leaves the default.  Always returns HDP_OK.
+ */
+hdp_status_t hdp_set_wait_budget(int64_t clocks);
 
 /* ====================================================================== */
 /* Cost models (host arithmetic only: no device, no stream, no allocation).

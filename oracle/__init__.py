@@ -21,6 +21,7 @@ from .oracle import (  # noqa: F401
     attention_bwd,
     attention_bwd_dq_rows,
     attention_bwd_dkv_rows,
+    attention_bwd_dkv_doc,
     bf16_bits_to_f64,
     merge,
     flops_total,

@@ -559,6 +559,78 @@ int oracle_attention_bwd(const double* q, const double* k, const double* v, cons
   return err;
 }
 
+/* dk and dv of selected keys of one document for one kv head g: the same sums
+ * as oracle_attention_bwd (over the group's query heads h and the document's
+ * queries a >= key), arranged by query row so that each row's softmax and dS
+ * are computed once for all the selected keys.  keys[i] are doc-local
+ * positions.  The rows are split over the threads; each thread sums into its
+ * own buffer and the buffers are added in thread order at the end. */
+int oracle_attention_bwd_dkv_doc(const double* q, const double* k, const double* v, const double* dout,
+                                 const int32_t* cu_seqlens, int32_t n, int32_t hq, int32_t hkv, int32_t d,
+                                 double scale, int32_t doc, int32_t g, const int64_t* keys, int64_t nk,
+                                 double* dk_out, double* dv_out) {
+  if (check_heads(hq, hkv, d) != ORC_OK || n < 1 || doc < 0 || doc >= n || g < 0 || g >= hkv || nk < 1)
+    return ORC_EINVAL;
+  const int64_t start = cu_seqlens[doc], end = cu_seqlens[doc + 1], len = end - start;
+  int64_t kmin = len;
+  for (int64_t i = 0; i < nk; i++) {
+    if (keys[i] < 0 || keys[i] >= len) return ORC_EINVAL;
+    if (keys[i] < kmin) kmin = keys[i];
+  }
+  const int32_t grp = hq / hkv;
+  const int nthreads = omp_get_max_threads();
+  const size_t per = (size_t)nk * (size_t)d * 2;
+  double* acc = (double*)calloc(per * (size_t)nthreads, sizeof(double));
+  if (!acc) return ORC_ENOMEM;
+  int err = ORC_OK;
+  const int64_t rows = (int64_t)grp * (len - kmin);
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)len);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)len);
+    double* dq_a = (double*)malloc(sizeof(double) * (size_t)d);
+    double* mine = acc + per * (size_t)omp_get_thread_num();
+    if (!p || !ds || !dq_a) {
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 8)
+      for (int64_t r = 0; r < rows; r++) {
+        const int32_t h = g * grp + (int32_t)(r / (len - kmin));
+        const int64_t a = start + kmin + r % (len - kmin);
+        bwd_row(q, k, v, dout, hq, hkv, d, scale, start, a, h, p, ds, dq_a);
+        const double* qa = q + (a * hq + h) * (int64_t)d;
+        const double* doa = dout + (a * hq + h) * (int64_t)d;
+        for (int64_t i = 0; i < nk; i++) {
+          const int64_t j = keys[i];
+          if (start + j > a) continue;  /* key after the query: masked */
+          double* dkb = mine + (size_t)i * d * 2;
+          double* dvb = dkb + d;
+          for (int32_t c = 0; c < d; c++) {
+            dkb[c] += scale * ds[j] * qa[c];
+            dvb[c] += p[j] * doa[c];
+          }
+        }
+      }
+    }
+    free(p);
+    free(ds);
+    free(dq_a);
+  }
+  for (int64_t i = 0; i < nk; i++)
+    for (int32_t c = 0; c < d; c++) {
+      double sk = 0.0, sv = 0.0;
+      for (int t = 0; t < nthreads; t++) {
+        sk += acc[per * (size_t)t + (size_t)i * d * 2 + c];
+        sv += acc[per * (size_t)t + (size_t)i * d * 2 + d + c];
+      }
+      dk_out[i * d + c] = sk;
+      dv_out[i * d + c] = sv;
+    }
+  free(acc);
+  return err;
+}
+
 /* Sampled dq rows: dq_out[i] = dq of token tokens[i], query head heads[i]. */
 int oracle_attention_bwd_dq_rows(const double* q, const double* k, const double* v, const double* dout,
                                  const int32_t* cu_seqlens, int32_t n, int32_t hq, int32_t hkv, int32_t d,

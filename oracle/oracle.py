@@ -53,6 +53,8 @@ def _load():
             lib.oracle_attention_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, P]
             lib.oracle_attention_bwd_dq_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, i64, P]
             lib.oracle_attention_bwd_dkv_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, P, i64, P, P]
+            lib.oracle_attention_bwd_dkv_doc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, i64,
+                                                         P, P]
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -252,6 +254,24 @@ def attention_bwd_dkv_rows(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int,
                                            float(scale), _ptr(t), _ptr(g), len(t), _ptr(dk), _ptr(dv))
     if rc != 0:
         raise ValueError(f"oracle_attention_bwd_dkv_rows failed (rc={rc})")
+    return dk, dv
+
+
+def attention_bwd_dkv_doc(q, k, v, dout, cu_seqlens, hq: int, hkv: int, d: int, scale: float, doc: int, kv_head: int,
+                          keys):
+    """dk and dv of selected doc-local keys of one document and kv head,
+    fp64 [nk][d] each (each query row computed once for all the keys)."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    kk = np.ascontiguousarray(keys, np.int64)
+    dk = np.zeros((len(kk), d), np.float64)
+    dv = np.zeros((len(kk), d), np.float64)
+    rc = lib.oracle_attention_bwd_dkv_doc(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(cu), len(cu) - 1, hq, hkv, d,
+                                          float(scale), int(doc), int(kv_head), _ptr(kk), len(kk), _ptr(dk),
+                                          _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dkv_doc failed (rc={rc})")
     return dk, dv
 
 

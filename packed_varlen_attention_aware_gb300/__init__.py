@@ -38,6 +38,8 @@ from .binding import (  # noqa: F401
     hdp_fit_cost_model,
     hdp_flops_per_shard,
     hdp_kernel_launch_count,
+    hdp_host_sync_count,
+    hdp_set_wait_budget,
     hdp_last_error_message,
     hdp_lse_merge,
     hdp_lse_merge_rows,

@@ -31,7 +31,7 @@ EXPORTED = (
     "hdp_plan_create", "hdp_plan_create_ex", "hdp_plan_view", "hdp_plan_destroy",
     "hdp_attention_workspace_bytes", "hdp_attention_fwd", "hdp_lse_merge", "hdp_lse_merge_rows",
     "hdp_flops_per_shard", "hdp_device_status", "hdp_status_string", "hdp_last_error_message",
-    "hdp_kernel_launch_count", "hdp_attention_fwd_split_noalloc",
+    "hdp_kernel_launch_count", "hdp_host_sync_count", "hdp_set_wait_budget", "hdp_attention_fwd_split_noalloc",
     "hdp_ring_step_compute", "hdp_ring_attention_time", "hdp_offload_ranks", "hdp_fit_cost_model",
     "hdp_balance_schedule", "hdp_attention_bwd_workspace_bytes", "hdp_attention_bwd",
 )
@@ -90,6 +90,7 @@ def load(path: str | None = None):
             "hdp_lse_merge_rows": [I32, I64, I32, V, V, V, V, V],
             "hdp_flops_per_shard": [V, I32, I32, V, V],
             "hdp_device_status": [V],
+            "hdp_set_wait_budget": [I64],
             "hdp_status_string": [ctypes.c_int],
             "hdp_last_error_message": [],
             "hdp_ring_step_compute": [V, I32, I32, I32, ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
@@ -107,6 +108,8 @@ def load(path: str | None = None):
             f.restype = ctypes.c_int
         lib.hdp_kernel_launch_count.argtypes = []
         lib.hdp_kernel_launch_count.restype = ctypes.c_uint64
+        lib.hdp_host_sync_count.argtypes = []
+        lib.hdp_host_sync_count.restype = ctypes.c_uint64
         lib.hdp_status_string.restype = ctypes.c_char_p
         lib.hdp_last_error_message.restype = ctypes.c_char_p
         _lib = lib
@@ -288,6 +291,14 @@ def hdp_status_string(status: int) -> str:
 
 def hdp_kernel_launch_count() -> int:
     return int(load().hdp_kernel_launch_count())
+
+
+def hdp_host_sync_count() -> int:
+    return int(load().hdp_host_sync_count())
+
+
+def hdp_set_wait_budget(clocks: int) -> None:
+    _check(load().hdp_set_wait_budget(int(clocks)), "hdp_set_wait_budget")
 
 
 def hdp_last_error_message() -> str:

@@ -7,6 +7,7 @@
 #include <string>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 thread_local std::string g_last_error;
@@ -14,12 +15,16 @@ __device__ unsigned int g_device_error;  // 0 = ok, else a code from the kernels
 
 std::mutex g_mu;
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<unsigned long long> g_host_syncs{0};
+std::atomic<long long> g_wait_budget{hdp::kWaitBudgetClocks};
 unsigned int* g_err_ptr[64] = {nullptr};
 }  // namespace
 
 namespace hdp {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void note_host_sync() { g_host_syncs.fetch_add(1, std::memory_order_relaxed); }
+long long wait_budget_clocks() { return g_wait_budget.load(std::memory_order_relaxed); }
 
 hdp_status_t fail(hdp_status_t st, const std::string& msg) {
   g_last_error = msg;
@@ -64,8 +69,17 @@ const char* hdp_last_error_message(void) { return g_last_error.c_str(); }
 
 uint64_t hdp_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t hdp_host_sync_count(void) { return g_host_syncs.load(std::memory_order_relaxed); }
+
+hdp_status_t hdp_set_wait_budget(int64_t clocks) {
+  g_wait_budget.store(clocks > 0 ? static_cast<long long>(clocks) : hdp::kWaitBudgetClocks,
+                      std::memory_order_relaxed);
+  return HDP_OK;
+}
+
 hdp_status_t hdp_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  hdp::note_host_sync();
   HDP_CUDA_TRY(cudaStreamSynchronize(s));
   unsigned int* w = hdp::device_error_word();
   if (!w) return hdp::fail(HDP_ERR_CUDA, "cannot resolve the device error word");

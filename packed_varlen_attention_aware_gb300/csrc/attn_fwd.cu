@@ -99,6 +99,7 @@ struct Params {
   int C;
   int split;
   unsigned int* err;
+  long long wait_budget;  // clocks before a role's wait gives up (drain waits keep their own budget)
 };
 
 struct Unit {
@@ -212,13 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kj >= 0) {
           const long long round = kload / kStages;
           if (round > 0 &&
-              !mbar_wait(&bars.k_empty[kload % kStages], (round - 1) & 1, abort_word, p.err, kErrKEmpty))
+              !mbar_wait(&bars.k_empty[kload % kStages], (round - 1) & 1, abort_word, p.err, kErrKEmpty,
+                         p.wait_budget))
             return false;
         }
         if (vj >= 0) {
           const long long round = vload / kStages;
           if (round > 0 &&
-              !mbar_wait(&bars.v_empty[vload % kStages], (round - 1) & 1, abort_word, p.err, kErrVEmpty))
+              !mbar_wait(&bars.v_empty[vload % kStages], (round - 1) & 1, abort_word, p.err, kErrVEmpty,
+                         p.wait_budget))
             return false;
         }
         // A group barrier is re-armed only after the MMA thread has consumed
@@ -226,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and re-arming earlier could complete two phases before the MMA thread
         // looks, which it would then miss.
         uint64_t* bar = &bars.kv_full[g & 1];
-        if (g >= 2 && !mbar_wait(&bars.kv_empty[g & 1], ((g >> 1) - 1) & 1, abort_word, p.err, kErrKvEmpty))
+        if (g >= 2 && !mbar_wait(&bars.kv_empty[g & 1], ((g >> 1) - 1) & 1, abort_word, p.err, kErrKvEmpty,
+                                 p.wait_budget))
           return false;
         mbar_arrive_expect_tx(bar, (kj >= 0 ? L::kTileBytes : 0) + (vj >= 0 ? L::kTileBytes : 0));
         if (kj >= 0) {
@@ -253,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit x = load_unit(p, u);
         for (int s = 0; s < 2 && ok; ++s) {
           if (s == 1 && !x.valid1) continue;
-          if (q_uses[s] > 0) ok = mbar_wait(&bars.q_empty[s], (q_uses[s] - 1) & 1, abort_word, p.err, kErrQEmpty);
+          if (q_uses[s] > 0)
+            ok = mbar_wait(&bars.q_empty[s], (q_uses[s] - 1) & 1, abort_word, p.err, kErrQEmpty, p.wait_budget);
           if (!ok) break;
           ++q_uses[s];
           uint8_t* dst = smem + L::kQ + s * L::kTileBytes;
@@ -265,13 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = arm_group(x, 0, -1);
         for (int j = 0; j < x.ntiles_kv && ok; ++j) ok = arm_group(x, j + 1 < x.ntiles_kv ? j + 1 : -1, j);
       }
-      if (!ok) {
-        // drain: every armed group barrier completes once its bytes land
-        for (int b = 0; b < 2; ++b)
-          if (gcount[b] > 0) drain_wait(&bars.kv_full[b], (gcount[b] - 1) & 1);
-        for (int s = 0; s < 2; ++s)
-          if (q_uses[s] > 0) drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
-      }
+      // Drain: every armed barrier's last phase completes once its bytes
+      // land, so no copy into this CTA's shared memory is still in flight when
+      // it exits, also when another role gave up after this loop ended.  In a
+      // normal run these phases completed long ago and each wait returns at
+      // its first poll.
+      for (int b = 0; b < 2; ++b)
+        if (gcount[b] > 0) drain_wait(&bars.kv_full[b], (gcount[b] - 1) & 1);
+      for (int s = 0; s < 2; ++s)
+        if (q_uses[s] > 0) drain_wait(&bars.q_full[s], (q_uses[s] - 1) & 1);
     }
     __syncwarp();
     tc_fence_before();
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long g = 0;
     bool ok = true;  // the waiter's own waits so far
     auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
-      if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code);
+      if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code, p.wait_budget);
     };
     auto wait_group = [&](int code) {  // one TMA group; the producer may re-arm its barrier afterwards
       wait_on(&bars.kv_full[g & 1], (g >> 1) & 1, code);
@@ -450,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key_limit = min(q_rel + 1, x.kv_len);  // keys [0, key_limit) are allowed
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < x.ntiles_kv && ok; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[s], s_count & 1, abort_word, p.err, kErrSFull));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars.s_full[s], s_count & 1, abort_word, p.err, kErrSFull, p.wait_budget));
         if (!ok) break;
         ++s_count;
         tc_fence_after();
@@ -537,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: wait for the unit's last P.V, normalize, store
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[s], units_done & 1, abort_word, p.err, kErrOFull));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bars.o_full[s], units_done & 1, abort_word, p.err, kErrOFull, p.wait_budget));
       if (!ok) break;
       tc_fence_after();
       const bool row_valid = row < x.q_rows;
@@ -665,6 +674,7 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   prm.split = split ? 1 : 0;
   prm.err = device_error_word();
   if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
+  prm.wait_budget = wait_budget_clocks();
   const long long units = prm.ntiles * hkv * prm.npairs;
   if (units == 0) return HDP_OK;
   int dev = 0, sms = 0;
@@ -741,13 +751,13 @@ extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const 
 }
 
 // ---------------------------------------------------------------- SPLIT without allocation
-// Some callers cannot allocate device memory when they run attention: code
-// that executes while a CUDA graph is being captured (cudaMalloc cannot be
-// captured), serving processes that reserve all device memory up front and
-// forbid allocation on the request path, and callers that must not take the
-// device-wide synchronisation cudaMalloc/cudaFree may imply.  For them SPLIT
-// mode can use a fixed scratch area that is part of the library image instead
-// of a caller-provided workspace.
+// Some callers cannot allocate device memory when they run attention:
+// serving processes that reserve all device memory at start-up and forbid
+// allocation on the request path, host programs whose own allocator owns the
+// device memory, and callers that must not take the device-wide
+// synchronisation cudaMalloc/cudaFree may imply.  For them SPLIT mode can use
+// a fixed scratch array that is part of the library image instead of a
+// caller-provided workspace.
 namespace hdp {
 namespace {
 

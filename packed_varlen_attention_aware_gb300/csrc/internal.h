@@ -27,6 +27,12 @@ unsigned int* device_error_word();
 
 // Count one kernel enqueued by this library (reported by hdp_kernel_launch_count).
 void note_launch();
+// Count one host wait on a stream (reported by hdp_host_sync_count).
+void note_host_sync();
+
+// Budget, in SM clocks, of the attention forward's role waits (set by
+// hdp_set_wait_budget; the default is about one second).
+long long wait_budget_clocks();
 
 }  // namespace hdp
 

@@ -292,13 +292,13 @@ __device__ __forceinline__ int32_t upper_doc(const T* __restrict__ off, int32_t 
   return lo;
 }
 
-// Chunk table, causal pairs per chunk, and the shard of every full chunk
-// (full chunks take shard ids in chunk order: chunk c of document i is
-// preceded by po[i] sub-capacity pieces).
+// Chunk table, causal pairs per chunk, and the shard of every chunk: full
+// chunks take shard ids in chunk order (chunk c of document i is preceded by
+// po[i] sub-capacity pieces); a piece takes the shard best fit gave it.
 __global__ void k_fill_chunks(int32_t n, int32_t C, long long nc, const int32_t* __restrict__ cu,
                               const int32_t* __restrict__ co, const int32_t* __restrict__ po,
-                              int32_t* __restrict__ chunk_table, int64_t* __restrict__ chunk_pairs,
-                              int32_t* __restrict__ shard_of_chunk) {
+                              const int32_t* __restrict__ piece_shard, int32_t* __restrict__ chunk_table,
+                              int64_t* __restrict__ chunk_pairs, int32_t* __restrict__ shard_of_chunk) {
   for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < nc;
        c += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int32_t doc = upper_doc(co, n, c);
@@ -314,7 +314,7 @@ __global__ void k_fill_chunks(int32_t n, int32_t C, long long nc, const int32_t*
     row.w = static_cast<int32_t>(len);
     reinterpret_cast<int4*>(chunk_table)[c] = row;
     chunk_pairs[c] = (b * (b + 1) - a * (a + 1)) / 2;
-    if (shard_of_chunk && len == C) shard_of_chunk[c] = static_cast<int32_t>(c - po[doc]);
+    if (shard_of_chunk) shard_of_chunk[c] = len == C ? static_cast<int32_t>(c - po[doc]) : piece_shard[doc];
   }
 }
 
@@ -497,17 +497,18 @@ __global__ void k_gather_rows(const unsigned long long* __restrict__ keys, long 
 }
 
 // ---------------------------------------------------------------- best fit
-// Key of a sub-capacity piece: (C - len) << 32 | doc, so ascending order is
-// length descending, then document ascending.
-__global__ void k_piece_keys(int32_t n, int32_t C, const int32_t* __restrict__ cu, const int32_t* __restrict__ po,
+// Key of document i: its sub-capacity piece (short document or tail chunk) as
+// (C - len) << 32 | i, so ascending order is length descending, then document
+// ascending; documents without a piece (s a multiple of C, or an invalid
+// length) get ~0 and sort after every piece.
+__global__ void k_piece_keys(int32_t n, int32_t C, const int32_t* __restrict__ lengths,
                              unsigned long long* __restrict__ keys) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    if (po[i + 1] != po[i]) {
-      const int32_t s = cu[i + 1] - cu[i];
-      const int32_t last = s % C;  // non-zero here
-      keys[po[i]] = (static_cast<unsigned long long>(C - last) << 32) | static_cast<unsigned long long>(i);
-    }
+    const int32_t s = lengths[i];
+    const int32_t last = s >= 1 ? s % C : 0;
+    keys[i] = last != 0 ? (static_cast<unsigned long long>(C - last) << 32) | static_cast<unsigned long long>(i)
+                        : ~0ull;
   }
 }
 
@@ -516,12 +517,22 @@ constexpr int kBfdThreads = 1024;
 // Best fit over the pieces in sorted order: each goes to the open piece shard
 // with the least remaining capacity that still fits (lowest id on ties), else
 // opens a new shard.  Piece shards are numbered after the full-chunk shards.
-__global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long long* __restrict__ keys,
-                                                           int32_t npieces, int32_t C, int32_t nfull,
-                                                           const int32_t* __restrict__ co,
+// The piece and chunk counts come from the scan's totals on the device, so
+// the plan's one host read-back carries the shard count too: totals[kPartial]
+// becomes the number of shards, or -1 when there are more than kMaxPieces
+// pieces (nothing else is written then).  piece_shard[doc] receives the shard
+// of the document's piece.
+__global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long long* __restrict__ keys, int32_t C,
+                                                           long long* __restrict__ totals,
                                                            int32_t* __restrict__ remaining,
-                                                           int32_t* __restrict__ shard_of_chunk,
-                                                           int32_t* __restrict__ num_shards) {
+                                                           int32_t* __restrict__ piece_shard) {
+  const long long npc_total = totals[5];
+  const int32_t nfull = static_cast<int32_t>(totals[1] - npc_total);
+  if (npc_total > kMaxPieces || totals[7]) {
+    if (threadIdx.x == 0) totals[kPartial] = -1;
+    return;
+  }
+  const int32_t npieces = static_cast<int32_t>(npc_total);
   __shared__ unsigned long long wbest[kBfdThreads / 32];
   __shared__ int32_t s_open;
   if (threadIdx.x == 0) s_open = 0;
@@ -573,11 +584,11 @@ __global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long l
         sid = static_cast<int32_t>(best & 0xffffffffu);
         remaining[sid] -= len;
       }
-      shard_of_chunk[co[doc + 1] - 1] = nfull + sid;
+      piece_shard[doc] = nfull + sid;
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) *num_shards = nfull + s_open;
+  if (threadIdx.x == 0) totals[kPartial] = nfull + s_open;
 }
 
 // ---------------------------------------------------------------- FLOPs
@@ -649,7 +660,12 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   const int32_t n = num_docs;
   const int nblk = static_cast<int>((static_cast<long long>(n) + kScanTile - 1) / kScanTile);
 
-  // ---- phase 1: per-document offsets (sizes known from n)
+  // ---- phase 1: per-document offsets and best-fit shards (sizes known from n)
+  // Every sub-capacity piece belongs to one document, so the pieces' sort keys,
+  // the best-fit state and the per-document piece shards are sized by n and
+  // run before the one host read-back, which then carries the shard count.
+  const bool shards = !(flags & HDP_PLAN_NO_SHARDS);
+  const long long n2p = shards ? next_pow2(n < 2 ? 2 : n) : 0;
   size_t off = 0;
   const size_t o_cu = off; off = align256(off + sizeof(int32_t) * (n + 1));
   const size_t o_co = off; off = align256(off + sizeof(int32_t) * (n + 1));
@@ -657,15 +673,20 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   const size_t o_tof = off; off = align256(off + sizeof(int64_t) * (n + 1));
   const size_t o_tos = off; off = align256(off + sizeof(int64_t) * (n + 1));
   const size_t bytes1 = off;
-  const size_t o_po = 0;  // scratch: piece offsets, CTA partials, totals
+  const size_t o_po = 0;  // scratch: piece offsets, CTA partials, totals, best-fit state
   size_t soff = align256(sizeof(int32_t) * (n + 1));
   const size_t o_part = soff; soff = align256(soff + sizeof(long long) * kPartial * nblk);
-  const size_t o_tot = soff; soff = align256(soff + sizeof(long long) * kPartial);
+  const size_t o_tot = soff; soff = align256(soff + sizeof(long long) * (kPartial + 1));
+  const size_t o_pkey = soff; soff = align256(soff + sizeof(unsigned long long) * n2p);
+  const size_t o_rem = soff; soff = align256(soff + (shards ? sizeof(int32_t) * std::min<long long>(n, kMaxPieces) : 0));
+  const size_t o_psh = soff; soff = align256(soff + (shards ? sizeof(int32_t) * n : 0));
   const size_t sbytes = soff;
 
+  int device = 0;
+  HDP_CUDA_TRY(cudaGetDevice(&device));
   auto* plan = new (std::nothrow) hdp_plan_s;
   if (!plan) return fail(HDP_ERR_OUT_OF_MEMORY, "hdp_plan_create: host allocation failed");
-  HDP_CUDA_TRY(cudaGetDevice(&plan->device));
+  plan->device = device;
   plan->stream = st;
   plan->flags = flags;
   char* scratch = nullptr;
@@ -689,6 +710,9 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   int32_t* po = reinterpret_cast<int32_t*>(scratch + o_po);
   long long* partials = reinterpret_cast<long long*>(scratch + o_part);
   long long* totals = reinterpret_cast<long long*>(scratch + o_tot);
+  auto* pkeys = reinterpret_cast<unsigned long long*>(scratch + o_pkey);
+  auto* rem = reinterpret_cast<int32_t*>(scratch + o_rem);
+  auto* piece_shard = reinterpret_cast<int32_t*>(scratch + o_psh);
 
   k_plan_reduce<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials);
   note_launch();
@@ -697,24 +721,35 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   k_plan_scan_write<<<nblk, kScanThreads, 0, st>>>(d_lengths, n, capacity, split_ok, partials, cu, co, bo, tof,
                                                    tos, po);
   note_launch();
+  if (shards) {
+    k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, d_lengths, pkeys);
+    note_launch();
+    e = sort_keys(pkeys, n, st);
+    if (e != cudaSuccess) return cleanup(fail_cuda(e, "piece sort"));
+    k_shard_bfd<<<1, kBfdThreads, 0, st>>>(pkeys, capacity, totals, rem, piece_shard);
+    note_launch();
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "plan scan launch"));
-  long long h_tot[kPartial];
+  long long h_tot[kPartial + 1];
   e = cudaMemcpyAsync(h_tot, totals, sizeof h_tot, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) {
+    note_host_sync();
+    e = cudaStreamSynchronize(st);
+  }
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "plan totals readback"));
 
-  const long long T = h_tot[0], nc = h_tot[1], nb = h_tot[2], ntf = h_tot[3], nts = h_tot[4], npc = h_tot[5];
+  const long long T = h_tot[0], nc = h_tot[1], nb = h_tot[2], ntf = h_tot[3], nts = h_tot[4];
   if (h_tot[7]) return cleanup(fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: every length must be >= 1"));
   if (T >= (1ll << 31))
     return cleanup(fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: total tokens must be < 2^31"));
   if (nb >= (1ll << 31) || nts >= (1ll << 31))
     return cleanup(fail(HDP_ERR_UNSUPPORTED, "hdp_plan_create: more than 2^31 causal blocks or split tiles"));
-  const bool shards = !(flags & HDP_PLAN_NO_SHARDS);
-  if (shards && npc > kMaxPieces)
+  if (shards && h_tot[kPartial] < 0)
     return cleanup(fail(HDP_ERR_UNSUPPORTED,
                         "hdp_plan_create: more than 65536 sub-capacity pieces for best-fit packing "
                         "(use HDP_PLAN_NO_SHARDS)"));
+  const int32_t h_ns = shards ? static_cast<int32_t>(h_tot[kPartial]) : 0;
 
   // ---- phase 2: tables sized by the totals
   off = 0;
@@ -724,7 +759,6 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   const size_t o_sc = off; off = align256(off + (shards ? sizeof(int32_t) * nc : 0));
   const size_t o_tf = off; off = align256(off + sizeof(int32_t) * 8 * ntf);
   const size_t o_ts = off; off = align256(off + sizeof(int32_t) * 8 * nts);
-  const size_t o_ns = off; off = align256(off + sizeof(int32_t));
   const size_t bytes2 = off;
   e = cudaMallocAsync(&plan->mem, bytes2, st);
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan tables)"));
@@ -735,30 +769,27 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   int32_t* shard_of_chunk = shards ? reinterpret_cast<int32_t*>(m2 + o_sc) : nullptr;
   int32_t* tiles_f = reinterpret_cast<int32_t*>(m2 + o_tf);
   int32_t* tiles_s = split_ok ? reinterpret_cast<int32_t*>(m2 + o_ts) : nullptr;
-  int32_t* d_ns = reinterpret_cast<int32_t*>(m2 + o_ns);
 
   // sort scratch: keys (power of two) + unsorted rows
-  const long long sort_n = std::max({ntf, split_ok ? nts : 0ll, shards ? npc : 0ll, 2ll});
+  const long long sort_n = std::max({ntf, split_ok ? nts : 0ll, 2ll});
   const long long n2 = next_pow2(sort_n);
   const long long nrows = std::max(ntf, split_ok ? nts : 0ll);
   char* sort_mem = nullptr;
   const size_t o_keys = 0;
   size_t so = align256(sizeof(unsigned long long) * n2);
   const size_t o_rows = so; so = align256(so + sizeof(int32_t) * 8 * nrows);
-  const size_t o_rem = so; so = align256(so + sizeof(int32_t) * (npc > 0 ? npc : 1));
   e = cudaMallocAsync(reinterpret_cast<void**>(&sort_mem), so, st);
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan sort scratch)"));
   auto* keys = reinterpret_cast<unsigned long long*>(sort_mem + o_keys);
   auto* rows = reinterpret_cast<int32_t*>(sort_mem + o_rows);
-  auto* rem = reinterpret_cast<int32_t*>(sort_mem + o_rem);
   auto cleanup2 = [&](hdp_status_t s) {
     cudaFreeAsync(sort_mem, st);
     return cleanup(s);
   };
 
   if (nc > 0) {
-    k_fill_chunks<<<grid_for(nc, 256), 256, 0, st>>>(n, capacity, nc, cu, co, po, chunk_table, chunk_pairs,
-                                                     shard_of_chunk);
+    k_fill_chunks<<<grid_for(nc, 256), 256, 0, st>>>(n, capacity, nc, cu, co, po, piece_shard, chunk_table,
+                                                     chunk_pairs, shard_of_chunk);
     note_launch();
   }
   if (nb > 0) {
@@ -781,25 +812,8 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
     k_gather_rows<<<grid_for(nts, 256), 256, 0, st>>>(keys, nts, rows, tiles_s);
     note_launch();
   }
-  int32_t h_ns = 0;
-  if (shards) {
-    if (npc > 0) {
-      k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, cu, po, keys);
-      note_launch();
-      e = sort_keys(keys, npc, st);
-      if (e != cudaSuccess) return cleanup2(fail_cuda(e, "piece sort"));
-    }
-    k_shard_bfd<<<1, kBfdThreads, 0, st>>>(keys, static_cast<int32_t>(npc), capacity,
-                                           static_cast<int32_t>(nc - npc), co, rem, shard_of_chunk, d_ns);
-    note_launch();
-    e = cudaGetLastError();
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_ns, d_ns, sizeof h_ns, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return cleanup2(fail_cuda(e, "shard packing"));
-  } else {
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cleanup2(fail_cuda(e, "plan table launch"));
-  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cleanup2(fail_cuda(e, "plan table launch"));
   cudaFreeAsync(sort_mem, st);
   cudaFreeAsync(scratch, st);
 

@@ -48,12 +48,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 
 // Slow path of mbar_wait (kept out of line so the fast path stays short).
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, volatile int* abort_word,
-                                            unsigned int* g_err, int code) {
+                                            unsigned int* g_err, int code, long long budget) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_word) return false;
-    if (clock64() - t0 > kWaitBudgetClocks) {
+    if (clock64() - t0 > budget) {
       *abort_word = code;
       if (g_err) atomicCAS(g_err, 0u, static_cast<unsigned int>(code));
       return false;
@@ -63,13 +63,13 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, vola
 
 // Bounded wait for the phase with the given parity to complete.  `abort_word`
 // is a CTA-shared flag: when another role already gave up, return false at
-// once; on timeout, store `code` there (and into the global error word) and
-// return false.
+// once; after `budget` clocks, store `code` there (and into the global error
+// word) and return false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_word,
-                                          unsigned int* g_err, int code) {
+                                          unsigned int* g_err, int code, long long budget = kWaitBudgetClocks) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  return mbar_wait_slow(a, parity, abort_word, g_err, code);
+  return mbar_wait_slow(a, parity, abort_word, g_err, code, budget);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -163,6 +163,21 @@ def test_named_workload_sampled(name):
     rk, rv = oracle.attention_bwd_dkv_rows(qb, kb, vb, dob, cu, w.hq, w.hkv, w.d, scale, kt, kh)
     compare(f"{name} dk rows", dk.float().numpy()[kt, kh], rk)
     compare(f"{name} dv rows", dv.float().numpy()[kt, kh], rv)
+    if name == "mb32k":
+        # keys at the start, the middle and the end of the longest document:
+        # the early ones accumulate over every query tile of the document and
+        # every query head of the group inside one CTA's TMEM
+        i = int(np.argmax(lengths))
+        s, a = lengths[i], int(cu[i])
+        mid = s // 2
+        keys = np.array([0, 1, int(rng.integers(2, 128)), mid - 1, mid, mid + int(rng.integers(1, 128)),
+                         s - 129, s - 2, s - 1], np.int64)
+        doc_cu = np.array([0, s], np.int32)  # a document's gradients do not depend on its neighbours
+        for g in (0, int(rng.integers(1, w.hkv))):
+            rk, rv = oracle.attention_bwd_dkv_doc(qb[a:a + s], kb[a:a + s], vb[a:a + s], dob[a:a + s], doc_cu, w.hq,
+                                                  w.hkv, w.d, scale, 0, g, keys)
+            compare(f"{name} dk, doc {i} kv head {g}", dk.float().numpy()[a + keys, g], rk)
+            compare(f"{name} dv, doc {i} kv head {g}", dv.float().numpy()[a + keys, g], rv)
 
 
 def test_workspace_and_argument_checks():

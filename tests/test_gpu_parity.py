@@ -58,6 +58,32 @@ def test_plan_many_docs_multi_cta_scan():
     check_plan(lengths, 384, with_shards=False)
 
 
+def test_plan_create_blocks_the_host_once():
+    """One read-back carries the totals and the best-fit shard count; the
+    per-shard FLOPs need no host wait."""
+    w = wl.workload("mix1m")
+    dl = torch.tensor(w.lengths, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    for flags in (pkg.HDP_PLAN_DEFAULT, pkg.HDP_PLAN_NO_SHARDS):
+        n0 = pkg.hdp_host_sync_count()
+        plan = pkg.hdp_plan_create(dl, w.capacity, flags=flags)
+        assert pkg.hdp_host_sync_count() - n0 == 1
+        if flags == pkg.HDP_PLAN_DEFAULT:
+            assert plan.view.num_shards == oracle.plan(list(w.lengths), w.capacity)["num_shards"]
+            f = torch.empty(plan.view.num_shards, dtype=torch.int64, device="cuda")
+            pkg.hdp_flops_per_shard(plan, w.d, w.hq, f)
+            assert pkg.hdp_host_sync_count() - n0 == 1
+        plan.destroy()
+
+
+def test_plan_rejects_too_many_pieces_for_best_fit():
+    dl = torch.full((70000,), 3, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkg.HdpError) as e:
+        pkg.hdp_plan_create(dl, 8)
+    assert e.value.status == pkg.HDP_ERR_UNSUPPORTED
+    pkg.hdp_plan_create(dl, 8, flags=pkg.HDP_PLAN_NO_SHARDS).destroy()
+
+
 def test_plan_rejects_bad_lengths():
     dl = torch.tensor([5, 0, 3], dtype=torch.int32, device="cuda")
     with pytest.raises(pkg.HdpError) as e:

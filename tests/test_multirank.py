@@ -82,3 +82,34 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = argparse.Namespace(workload="tiny", seed=0, steps=1, warmup=3, gpus=2, mode="fused", cpu_seconds=0.1)
     assert bench.reference_arm(args, 1) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself (torchrun,
+    127.0.0.1); rank 0 alone prints, and the line's n_gpus is the world size.
+    The reference arm (the oracle on host cores) needs no GPU, so the launcher
+    runs here."""
+    import json
+    import subprocess
+
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                              "MASTER_PORT")}
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--workload",
+           "tiny", "--steps", "1", "--warmup", "3", "--ref-step-seconds", "0.2"]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_world_size(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("WORLD_SIZE", "3")
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("LOCAL_RANK", "0")
+    with pytest.raises(SystemExit):
+        bench.main(["--impl", "reference", "--gpus", "2", "--workload", "tiny"])

@@ -122,3 +122,37 @@ def test_document_independence_and_dq_rows():
     dk_r, dv_r = oracle.attention_bwd_dkv_rows(*packed, cu, hq, hkv, d, 0.35, kt, kh)
     assert np.allclose(dk_r, dk[kt, 0], rtol=1e-12, atol=1e-14)
     assert np.allclose(dv_r, dv[kt, 0], rtol=1e-12, atol=1e-14)
+
+
+def test_dkv_of_document_keys_against_finite_differences():
+    """dk, dv of chosen keys of one document (the per-document form used on
+    long documents) against central differences of the fp64 forward, and
+    against the whole-batch gradients."""
+    rng = np.random.default_rng(6)
+    hq, hkv, d = 4, 2, 3
+    lengths = [5, 12, 4]
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    q, k, v = _rand((T, hq, d), rng), _rand((T, hkv, d), rng), _rand((T, hkv, d), rng)
+    g = _rand((T, hq, d), rng)
+    scale = 0.45
+    keys = np.array([0, 6, 11, 3])
+    doc, kvh = 1, 1
+    dk, dv = oracle.attention_bwd_dkv_doc(q, k, v, g, cu, hq, hkv, d, scale, doc, kvh, keys)
+    eps = 1e-6
+    for i, j in enumerate(keys):
+        tok = cu[doc] + j
+        for name, x, grad in (("k", k, dk), ("v", v, dv)):
+            for c in range(d):
+                xp, xm = x.copy(), x.copy()
+                xp[tok, kvh, c] += eps
+                xm[tok, kvh, c] -= eps
+                args_p = {"k": k, "v": v}
+                args_m = dict(args_p)
+                args_p[name], args_m[name] = xp, xm
+                fd = (_loss(q, args_p["k"], args_p["v"], g, cu, hq, hkv, d, scale)
+                      - _loss(q, args_m["k"], args_m["v"], g, cu, hq, hkv, d, scale)) / (2 * eps)
+                assert abs(fd - grad[i, c]) <= 1e-7 * max(1.0, abs(fd)), (name, j, c, fd, grad[i, c])
+    _, dk_all, dv_all = oracle.attention_bwd(q, k, v, g, cu, hq, hkv, d, scale)
+    assert np.allclose(dk, dk_all[cu[doc] + keys, kvh], rtol=1e-12, atol=1e-14)
+    assert np.allclose(dv, dv_all[cu[doc] + keys, kvh], rtol=1e-12, atol=1e-14)

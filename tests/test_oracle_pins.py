@@ -76,6 +76,46 @@ def test_attention_equals_bruteforce_masked_softmax(lengths, hq, hkv, d, seed):
     assert np.max(np.abs(lse - L)) < 1e-12
 
 
+def _bruteforce_f64(Q, K, V, lengths, hq, hkv, scale):
+    """The same explicit-mask softmax on arbitrary fp64 inputs."""
+    T, _, d = Q.shape
+    doc = np.repeat(np.arange(len(lengths)), lengths)
+    pos = np.arange(T)
+    mask = (doc[:, None] == doc[None, :]) & (pos[None, :] <= pos[:, None])
+    O = np.zeros((T, hq, d))
+    L = np.zeros((hq, T))
+    for h in range(hq):
+        g = h // (hq // hkv)
+        S = np.where(mask, Q[:, h, :] @ K[:, g, :].T * scale, -np.inf)
+        L[h] = logsumexp(S, axis=1)
+        O[:, h, :] = np.exp(S - L[h][:, None]) @ V[:, g, :]
+    return O, L
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,seed", [
+    ([1, 6, 13, 2], 4, 2, 8, 0),
+    ([21], 3, 1, 5, 1),
+    ([9, 9, 1, 30], 2, 2, 16, 2),
+])
+def test_attention_f64_equals_bruteforce_masked_softmax(lengths, hq, hkv, d, seed):
+    """The fp64-input forward (the one the backward's finite differences
+    differentiate) against the explicit-mask softmax on inputs that are not
+    bf16-representable, and bit for bit against the bf16-input forward on
+    bf16 inputs."""
+    rng = np.random.default_rng(100 + seed)
+    T = sum(lengths)
+    Q, K, V = rng.normal(0, 1.3, (T, hq, d)), rng.normal(0, 1.3, (T, hkv, d)), rng.normal(0, 1, (T, hkv, d))
+    scale = 0.61
+    o, lse = oracle.attention_f64(Q, K, V, _cu(lengths), hq, hkv, d, scale)
+    O, L = _bruteforce_f64(Q, K, V, lengths, hq, hkv, scale)
+    assert np.max(np.abs(o - O)) < 1e-12
+    assert np.max(np.abs(lse - L)) < 1e-12
+    q, k, v = _rand_qkv(lengths, hq, hkv, d, seed)
+    o16, lse16 = oracle.attention(q, k, v, _cu(lengths), hq, hkv, d, scale)
+    o64, lse64 = oracle.attention_f64(q, k, v, _cu(lengths), hq, hkv, d, scale)
+    assert np.array_equal(o16, o64) and np.array_equal(lse16, lse64)
+
+
 def test_zero_keys_closed_form():
     """K = 0: every score is 0, so LSE_p = ln(p+1) and O_p = mean(v_0..v_p)."""
     lengths = [3, 20, 1, 9]
