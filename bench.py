@@ -80,7 +80,13 @@ def attn_kernel_source_sha256() -> str:
 # from the ncu captures summarised under profiles/, keyed by (workload, mode).
 # A figure is reported only while the attention kernel's device source hashes
 # to the value it was captured with.
-PROFILED_TRAFFIC = {}
+PROFILED_TRAFFIC = {
+    ("seq128k", "fused"): {
+        "kernel_source_sha256": "779f5298ce1b6f52a2967c58174205afe6461b30402e05377e8b3e908c957f58",
+        "dram_bytes_per_launch": 173530875648 + 1083252736,
+        "source": "ncu capture summarised in profiles/attn_fwd_seq128k.md",
+    },
+}
 
 
 class ClockSampler:
@@ -606,6 +612,23 @@ def our_arm(args, ws, rank, local):
     return 0
 
 
+def attn_only_mode(args):
+    """The attention call alone on --workload / --mode, plan made once: W
+    warm-up and K timed launches (CUDA events), one JSON line.  Small enough
+    to run under ncu on the 128K sequence."""
+    import torch
+
+    from packed_varlen_attention_aware_gb300 import build as native_build
+
+    native_build.build()
+    torch.cuda.set_device(0)
+    peaks, _ = load_peaks()
+    out = attention_only(args.workload, args.mode, args.seed, args.warmup, args.steps, torch.device("cuda", 0), peaks)
+    out["mode_of_run"] = "attn-only"
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def kernels_mode(args):
     """Secondary kernels: the plan on 2^24 random lengths and the LSE merge on
     16 partials of 2^20 rows (d = 128).  CUDA-event times per call; the merge
@@ -659,6 +682,44 @@ def kernels_mode(args):
     gbs = nbytes / (ms * 1e-3) / 1e9
     out["lse_merge"] = {"m": m, "rows": rows, "d": d, "ms_per_call": ms, "algorithmic_bytes": nbytes,
                         "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}
+    del o_parts, lse_parts, o, lse
+    # the SPLIT partials of the 131,072-token sequence (136 blocks), merged by
+    # hdp_lse_merge: per (row, head) m (4d + 4) bytes read and 2d + 4 written,
+    # m = q chunk + 1
+    from packed_varlen_attention_aware_gb300 import workloads as wl
+
+    w = wl.workload("seq128k", args.seed)
+    q, k, v = wl.qkv(w, device="cuda")
+    dl = torch.tensor(w.lengths, dtype=torch.int32, device="cuda")
+    plan = pkg.hdp_plan_create(dl, w.capacity)
+    wsb = pkg.hdp_attention_workspace_bytes(plan, w.hq, w.d, pkg.HDP_MODE_SPLIT)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(w.hq, w.total_tokens, dtype=torch.float32, device="cuda")
+    pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, pkg.HDP_MODE_SPLIT, ws, o, lse)
+    rows_total = plan.view.num_blocks * w.capacity
+    o_part = ws[: rows_total * w.hq * w.d * 4].view(torch.float32)
+    lse_off = (rows_total * w.hq * w.d * 4 + 255) // 256 * 256
+    lse_part = ws[lse_off: lse_off + rows_total * w.hq * 4].view(torch.float32)
+    times = []
+    for it in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkg.hdp_lse_merge(plan, o_part, lse_part, w.hq, w.d, o, lse)
+        e1.record()
+        torch.cuda.synchronize()
+        if it:
+            times.append(e0.elapsed_time(e1))
+    pkg.hdp_device_status()
+    nch = plan.view.num_chunks
+    read = sum(w.capacity * w.hq * (qc + 1) * (4 * w.d + 4) for qc in range(nch))
+    written = w.total_tokens * w.hq * (2 * w.d + 4)
+    ms = statistics.median(times)
+    gbs = (read + written) / (ms * 1e-3) / 1e9
+    out["lse_merge_seq128k_split"] = {"blocks": plan.view.num_blocks, "ms_per_call": ms, "bytes_read": read,
+                                      "bytes_written": written, "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
+                                      "frac": gbs / peaks["hbm_gbs"]}
+    plan.destroy()
     print(json.dumps(out), flush=True)
     return 0
 
@@ -871,6 +932,7 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: CPU seconds per step (default: about 150 s over all steps)")
     ap.add_argument("--kernels", action="store_true", help="time the plan stress input and the LSE merge")
+    ap.add_argument("--attn-only", action="store_true", help="time the attention call alone on --workload")
     ap.add_argument("--cost-model", action="store_true",
                     help="calibrate T(s) and t_blk on this GPU and apply the ring model")
     ap.add_argument("--balance", action="store_true",
@@ -890,6 +952,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {ws}")
     if args.kernels:
         return kernels_mode(args) if rank == 0 else 0
+    if args.attn_only:
+        return attn_only_mode(args) if rank == 0 else 0
     if args.cost_model:
         return cost_model_mode(args) if rank == 0 else 0
     if args.balance:

@@ -213,6 +213,8 @@ hdp_status_t hdp_attention_bwd(hdp_plan_t plan, const void* q, const void* k, co
  * over the blocks (qc, kc), kc = 0..qc, of the chunk.
  *   o_part [N_b][C][hq][d] fp32, lse_part [N_b][hq][C] fp32 (the SPLIT
  *   workspace layout); o [T][hq][d] bf16, lse [hq][T] fp32.  d == 64 or 128.
+ *   The plan's capacity must be a multiple of 128 (as for SPLIT attention):
+ *   INVALID_ARGUMENT otherwise.
  */
 hdp_status_t hdp_lse_merge(hdp_plan_t plan, const float* o_part, const float* lse_part, int32_t hq, int32_t d,
                            void* o, float* lse, void* stream);
