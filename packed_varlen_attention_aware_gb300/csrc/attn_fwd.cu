@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
     long long g = 0;
-    bool ok = true;  // the waiter's own waits so far
+    bool ok = true;  // this thread's own waits so far
     auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
       if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code, p.wait_budget);
     };
@@ -362,13 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first P.V of a unit overwrites O_s, the previous epilogue's read
         if (waiter) {
           if (s == 0) wait_group(kErrVFull);
-          wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);
           if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
         }
         if (s == 0) ++g;
-        ++p_uses[s];
+        const uint32_t pu = p_uses[s]++;
         if (!handoff()) return false;
+        // P_s(j) is the last thing this slot's P.V needs, and the issuing
+        // thread has nothing to issue before it: it waits for it itself,
+        // which saves the waiter-to-issuer hop.  A failed wait reaches the
+        // waiter at the next handoff.
         if (issuer) {
+          ok = mbar_wait(&bars.p_full[s], pu & 1, abort_word, p.err, kErrPFull, p.wait_budget);
+          tc_fence_after();
+        }
+        if (issuer && ok) {
           issue_pv(s, vs, j > 0);
           if (kind == 2) {
             umma_commit(&bars.o_full[s]);
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (issuer) {
+      if (issuer && ok) {
         if (kind != 2) umma_commit(&bars.k_empty[ks]);
         umma_commit(&bars.v_empty[vs]);
       }
@@ -462,70 +469,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_count;
         tc_fence_after();
-        // S rows with their per-chunk maxima from the load itself.  A long
-        // arithmetic chain here would also take issue slots from the MMA warp,
-        // which shares a scheduler with one softmax warp of each slot.
+        const int lim = key_limit - j * kTile;  // allowed keys of this tile: [0, lim)
         uint32_t r[4][32];
         float mc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) mc[c] = tmem_ld32_max(tS(s) + lane_off + c * 32, r[c]);
-        tmem_wait_ld();
-        const int lim = key_limit - j * kTile;
-        if (lim < kTile) {
-          // tile crossing the diagonal or the end of the key range: mask, and
-          // take the maximum over the allowed keys only
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            mc[c] = __uint_as_float(r[c][0]);
-#pragma unroll
-            for (int i = 1; i < 31; i += 2)
-              mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-            mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
-          }
-        }
-        const float mt = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
-        const float mt_scaled = mt * p.scale_log2;
         bool rescale_o = false;
         float alpha = 1.f;
-        if (mt_scaled > m + kRescaleThreshold || j == 0) {
-          const float m_new = fmaxf(m, mt_scaled);
-          alpha = (j == 0) ? 0.f : ex2_approx(m - m_new);
-          l *= alpha;
-          m = m_new;
-          rescale_o = j > 0;
-        }
-        // p = 2^(s*scale*log2e - m); 16 independent packed partial sums, the
-        // four 32-column chunks interleaved element by element
-        const uint64_t negm2 = pack_f32x2(-m, -m);
-        uint64_t acc[16];
+        // p = 2^(s*scale*log2e - m) for one 32-column chunk: four packed
+        // partial row sums, P packed to bf16 pairs and stored into the first
+        // 64 columns of S (chunk c's keys land in columns [16c, 16c + 16)).
+        auto exp_chunk = [&](int c, uint64_t negm2, uint64_t (&acc)[4]) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc[q] = pack_f32x2(0.f, 0.f);
-        uint32_t pk[4][16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 32; i += 2) {
             const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])),
                                           scale2, negm2);
             const float p0 = ex2_approx(lo_f32(t));
             const float p1 = ex2_approx(hi_f32(t));
-            const int q = c * 4 + ((i >> 1) & 3);
-            acc[q] = fadd_f32x2(acc[q], pack_f32x2(p0, p1));
-            pk[c][i / 2] = pack_bf16x2(p0, p1);
+            acc[(i >> 1) & 3] = fadd_f32x2(acc[(i >> 1) & 3], pack_f32x2(p0, p1));
+            pk[i / 2] = pack_bf16x2(p0, p1);
           }
+          tmem_st16(tS(s) + lane_off + c * 16, pk);
+        };
+        auto row_sum = [](uint64_t (&acc)[4]) {
+          const uint64_t a = fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3]));
+          return lo_f32(a) + hi_f32(a);
+        };
+        if (__all_sync(0xffffffffu, j > 0 && lim >= kTile)) {
+          // Steady tile (no mask, running max known): each chunk's exponentials
+          // are computed with the running max while the next chunk's load is
+          // in flight; a chunk's P only overwrites S columns already loaded.
+          // The row maxima come from the loads themselves.  If one of them
+          // exceeds the running max by more than the threshold, the tile is
+          // recomputed from the registers with the new max (rare).
+          const uint64_t negm2 = pack_f32x2(-m, -m);
+          uint64_t acc[4] = {0, 0, 0, 0};
+          mc[0] = tmem_ld32_max(tS(s) + lane_off, r[0]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c < 3) mc[c + 1] = tmem_ld32_max(tS(s) + lane_off + (c + 1) * 32, r[c + 1]);
+            exp_chunk(c, negm2, acc);
+            if (c < 3) tmem_wait_ld();
+          }
+          const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
+          const bool grow = mt_scaled > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, grow)) {
+            if (grow) {
+              alpha = ex2_approx(m - mt_scaled);
+              l *= alpha;
+              m = mt_scaled;
+              rescale_o = true;
+            }
+            tmem_wait_st();  // the first pass's stores land before they are overwritten
+            const uint64_t negm2n = pack_f32x2(-m, -m);
+            uint64_t acc2[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) exp_chunk(c, negm2n, acc2);
+            l += row_sum(acc2);
+          } else {
+            l += row_sum(acc);
+          }
+        } else {
+          // first tile, or a tile crossing the diagonal or the end of the key
+          // range: load the whole row, mask, take the maximum over the allowed
+          // keys, then the exponentials
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mc[c] = tmem_ld32_max(tS(s) + lane_off + c * 32, r[c]);
+          tmem_wait_ld();
+          if (lim < kTile) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              mc[c] = __uint_as_float(r[c][0]);
+#pragma unroll
+              for (int i = 1; i < 31; i += 2)
+                mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+              mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+            }
+          }
+          const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
+          if (mt_scaled > m + kRescaleThreshold || j == 0) {
+            const float m_new = fmaxf(m, mt_scaled);
+            alpha = (j == 0) ? 0.f : ex2_approx(m - m_new);
+            l *= alpha;
+            m = m_new;
+            rescale_o = j > 0;
+          }
+          const uint64_t negm2 = pack_f32x2(-m, -m);
+          uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) exp_chunk(c, negm2, acc);
+          l += row_sum(acc);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_st16(tS(s) + lane_off + c * 16, pk[c]);
-#pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int q = 0; q < w; ++q) acc[q] = fadd_f32x2(acc[q], acc[q + w]);
-        l += lo_f32(acc[0]) + hi_f32(acc[0]);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // P.V of tile j-1 is complete: S_s(j) was committed after it
 #pragma unroll 1
