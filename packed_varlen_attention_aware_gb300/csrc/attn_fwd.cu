@@ -7,7 +7,7 @@
 // Design (one persistent CTA per SM, 12 warps):
 //   warps 0-3  softmax for query slot 0     warps 4-7  softmax for query slot 1
 //   warp 8     TMA producer                 warp 9     MMA issuer + TMEM owner
-//   warp 10    waits on behalf of the MMA issuer
+//   warps 10, 11 idle (they complete the control warpgroup)
 // A work unit is one query tile (128 rows of one document, from the plan's
 // heaviest-first work list) for one key/value head and a pair of query heads of
 // that head's GQA group: both slots share every K/V tile.  Only the key tiles
@@ -45,15 +45,13 @@ hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, co
 namespace {
 
 // 12 warps = 3 warpgroups: two softmax warpgroups and one for the producer
-// (warp 8), the MMA issuer (warp 9), its waiter (warp 10) and an idle warp.
+// (warp 8), the MMA issuer (warp 9) and two idle warps.
 // Launched at 168 registers a thread (384 x 168 = 64,512); setmaxnreg then moves registers to
 // the softmax warpgroups: 2 x 128 x 176 + 128 x 152 = 64,512 (the MMA
 // issuer's straight-line code needs the control share).
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kWaitWarp = 10;
-constexpr uint32_t kHandoffBarrier = 2;  // named barrier between the waiter and MMA warps
 constexpr int kSoftmaxRegs = 176;
 constexpr int kControlRegs = 152;
 constexpr int kStages = 2;  // K and V ring depth
@@ -283,99 +281,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     named_barrier_sync(1, kThreads);
-  } else if (warp == kMmaWarp || warp == kWaitWarp) {
-    // ------------------------------------------------------------ MMA issuer + waiter
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
     // Per key tile j: for each slot P.V(j) followed at once by S = Q K(j+1)^T.
     // S(j+1) of a slot overwrites the TMEM columns that P(j) of the same slot
     // occupies; one thread issues the two back to back and they execute in
     // issue order.
     //
-    // The tensor core's issue queue is shallow, and an mbarrier poll by the
-    // issuing thread lets it run dry.  So the waiter warp performs every
-    // mbarrier wait the MMA stream depends on, in the order the stream consumes
-    // them, and hands each finished wait to the MMA warp through a named
-    // barrier, which carries no such cost.  Both warps walk the same units and
-    // tiles and pass the same handoffs; the barrier also ORs a failure flag, so
-    // a timed-out wait stops both warps at the same handoff.
-    const bool issuer = warp == kMmaWarp && lane == 0;
-    const bool waiter = warp == kWaitWarp && lane == 0;
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-    // Descriptors: base per buffer; K steps add compile-time offsets to the
-    // start-address field (addresses stay below 256 KB, so no carry).
-    const uint64_t dQ = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-    const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
-    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-    const uint64_t dK1 = dK + kTileUnits, dV1 = dV + kTileUnits;
-    auto issue_qk = [&](int s, int kst) {
-      const uint64_t qd = dQ + s * kTileUnits, kd = kst ? dK1 : dK;
-      umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
-#pragma unroll
-      for (int kk = 1; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
-        umma_ss_c<true>(tS(s), qd + off, kd + off, idesc_qk);
-      }
-      umma_commit(&bars.s_full[s]);
-    };
-    auto issue_pv = [&](int s, int vst, bool accumulate) {
-      const uint64_t vd = vst ? dV1 : dV;
-      if (accumulate)
-        umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
-      else
-        umma_ts_c<false>(tO(s), tS(s), vd, idesc_pv);
-#pragma unroll
-      for (int kk = 1; kk < kTile / 16; ++kk)
-        umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
-    };
-    uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
-    long long g = 0;
-    bool ok = true;  // this thread's own waits so far
-    auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
-      if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code, p.wait_budget);
-    };
-    auto wait_group = [&](int code) {  // one TMA group; the producer may re-arm its barrier afterwards
-      wait_on(&bars.kv_full[g & 1], (g >> 1) & 1, code);
-      if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
-    };
-    // Both warps, all lanes.  True when every wait so far succeeded; the MMA
-    // warp then orders its next tcgen05 operations after the waits.
-    auto handoff = [&]() -> bool {
-      __syncwarp();
-      const bool failed = named_barrier_or(kHandoffBarrier, 64, !ok);
-      tc_fence_after();
-      return !failed;
-    };
-    // K and V stages advance together (n of each per unit), so one parity c
-    // per unit fixes them: P.V(j) reads V stage c ^ (j & 1), S(j+1) K stage
-    // c ^ 1 ^ (j & 1).  The steady key tiles are unrolled by two with those
-    // stages as constants, and the last two tiles are peeled, so the issuing
-    // thread runs straight-line code: per-MMA index arithmetic or commit
-    // branches inside its one-lane region cost it tens of cycles a MMA.
-    bool alive = true;
-    // key tile j of the unit; kind 0: steady (j < n - 2), 1: j = n - 2 (Q is
-    // free after its S), 2: j = n - 1 (the unit's last P.V)
-    auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind) -> bool {
-      for (int s = 0; s < nslots; ++s) {
-        // handoff: (slot 0) the group holding V(j) and K(j+1); P_s(j)
-        // written and O_s rescaled by the softmax warps; and, before the
-        // first P.V of a unit overwrites O_s, the previous epilogue's read
-        if (waiter) {
+    // The tensor core's queue holds only about two MMAs, so every cycle the
+    // issuing thread spends between two slots' MMA groups can leave it idle.
+    // The thread therefore does the few waits its MMAs depend on itself, at
+    // the group boundaries where it has nothing else to issue: the TMA group
+    // holding V(j) and K(j+1), the slot's P(j), and (first tile of a unit)
+    // the previous epilogue's read of O.  Each is one try-wait when already
+    // complete; a cross-warp hand-off here cost about 250 cycles a slot.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      // Descriptors: base per buffer; K steps add compile-time offsets to the
+      // start-address field (addresses stay below 256 KB, so no carry).
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + L::kV), L::kHalfBytes, 1024);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const uint64_t dK1 = dK + kTileUnits, dV1 = dV + kTileUnits;
+      auto issue_qk = [&](int s, int kst) {
+        const uint64_t qd = dQ + s * kTileUnits, kd = kst ? dK1 : dK;
+        umma_ss_c<false>(tS(s), qd, kd, idesc_qk);
+  #pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+          umma_ss_c<true>(tS(s), qd + off, kd + off, idesc_qk);
+        }
+        umma_commit(&bars.s_full[s]);
+      };
+      auto issue_pv = [&](int s, int vst, bool accumulate) {
+        const uint64_t vd = vst ? dV1 : dV;
+        if (accumulate)
+          umma_ts_c<true>(tO(s), tS(s), vd, idesc_pv);
+        else
+          umma_ts_c<false>(tO(s), tS(s), vd, idesc_pv);
+  #pragma unroll
+        for (int kk = 1; kk < kTile / 16; ++kk)
+          umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
+      };
+      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
+      long long g = 0;
+      bool ok = true;  // every wait so far succeeded
+      auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
+        if (ok) ok = mbar_wait(bar, parity, abort_word, p.err, code, p.wait_budget);
+      };
+      auto wait_group = [&](int code) {  // one TMA group; the producer may re-arm its barrier afterwards
+        wait_on(&bars.kv_full[g & 1], (g >> 1) & 1, code);
+        if (ok) mbar_arrive(&bars.kv_empty[g & 1]);
+        ++g;
+      };
+      // K and V stages advance together (n of each per unit), so one parity c
+      // per unit fixes them: P.V(j) reads V stage c ^ (j & 1), S(j+1) K stage
+      // c ^ 1 ^ (j & 1).  The steady key tiles are unrolled by two with those
+      // stages as constants, and the last two tiles are peeled, so the issuing
+      // thread runs straight-line code: per-MMA index arithmetic or commit
+      // branches cost it tens of cycles a MMA.
+      // key tile j of the unit; kind 0: steady (j < n - 2), 1: j = n - 2 (Q is
+      // free after its S), 2: j = n - 1 (the unit's last P.V)
+      auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind) -> bool {
+        for (int s = 0; s < nslots; ++s) {
           if (s == 0) wait_group(kErrVFull);
           if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
-        }
-        if (s == 0) ++g;
-        const uint32_t pu = p_uses[s]++;
-        if (!handoff()) return false;
-        // P_s(j) is the last thing this slot's P.V needs, and the issuing
-        // thread has nothing to issue before it: it waits for it itself,
-        // which saves the waiter-to-issuer hop.  A failed wait reaches the
-        // waiter at the next handoff.
-        if (issuer) {
-          ok = mbar_wait(&bars.p_full[s], pu & 1, abort_word, p.err, kErrPFull, p.wait_budget);
+          wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);  // P_s(j) written, O_s rescaled
+          ++p_uses[s];
+          if (!ok) return false;
           tc_fence_after();
-        }
-        if (issuer && ok) {
           issue_pv(s, vs, j > 0);
           if (kind == 2) {
             umma_commit(&bars.o_full[s]);
@@ -384,52 +360,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kind == 1) umma_commit(&bars.q_empty[s]);
           }
         }
-      }
-      if (issuer && ok) {
         if (kind != 2) umma_commit(&bars.k_empty[ks]);
         umma_commit(&bars.v_empty[vs]);
-      }
-      return true;
-    };
-    int c = 0;  // stage parity at the start of a unit
-    for (long long k = 0; alive; ++k) {
-      const long long u = unit_index(k, cta, nctas);
-      if (u >= total_units) break;
-      const Unit x = load_unit(p, u);
-      const int nslots = x.valid1 ? 2 : 1;
-      const int n = x.ntiles_kv;
-      // handoff: Q of every slot and the group holding K(0)
-      if (waiter) {
+        return true;
+      };
+      bool alive = true;
+      int c = 0;  // stage parity at the start of a unit
+      for (long long k = 0; alive; ++k) {
+        const long long u = unit_index(k, cta, nctas);
+        if (u >= total_units) break;
+        const Unit x = load_unit(p, u);
+        const int nslots = x.valid1 ? 2 : 1;
+        const int n = x.ntiles_kv;
+        // Q of every slot and the group holding K(0)
         for (int s = 0; s < nslots; ++s) wait_on(&bars.q_full[s], q_uses[s] & 1, kErrQFull);
+        for (int s = 0; s < nslots; ++s) ++q_uses[s];
         wait_group(kErrKFull);
-      }
-      for (int s = 0; s < nslots; ++s) ++q_uses[s];
-      ++g;
-      if (!handoff()) break;
-      if (issuer) {
+        if (!ok) break;
+        tc_fence_after();
         for (int s = 0; s < nslots; ++s) {
           issue_qk(s, c);
           if (n == 1) umma_commit(&bars.q_empty[s]);
         }
         umma_commit(&bars.k_empty[c]);
+        int j = 0;
+        if (c == 0) {
+          for (; j + 1 < n - 2 && alive; j += 2)
+            alive = tile(x, nslots, j, 0, 1, 0) && tile(x, nslots, j + 1, 1, 0, 0);
+        } else {
+          for (; j + 1 < n - 2 && alive; j += 2)
+            alive = tile(x, nslots, j, 1, 0, 0) && tile(x, nslots, j + 1, 0, 1, 0);
+        }
+        for (; j < n - 2 && alive; ++j) alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0);
+        if (alive && n >= 2) {
+          alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 1);
+          ++j;
+        }
+        if (alive) alive = tile(x, nslots, j, c ^ (j & 1), 0, 2);
+        if (!alive) break;
+        c ^= n & 1;
+        for (int s = 0; s < nslots; ++s) ++units_done[s];
       }
-      int j = 0;
-      if (c == 0) {
-        for (; j + 1 < n - 2 && alive; j += 2) alive = tile(x, nslots, j, 0, 1, 0) && tile(x, nslots, j + 1, 1, 0, 0);
-      } else {
-        for (; j + 1 < n - 2 && alive; j += 2) alive = tile(x, nslots, j, 1, 0, 0) && tile(x, nslots, j + 1, 0, 1, 0);
-      }
-      for (; j < n - 2 && alive; ++j) alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0);
-      if (alive && n >= 2) {
-        alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 1);
-        ++j;
-      }
-      if (alive) alive = tile(x, nslots, j, c ^ (j & 1), 0, 2);
-      if (!alive) break;
-      c ^= n & 1;
-      for (int s = 0; s < nslots; ++s) ++units_done[s];
-    }
-    if (issuer) {
       // drain every MMA this thread issued before TMEM is released
       umma_commit(&bars.drain);
       drain_wait(&bars.drain, 0);
@@ -437,12 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     named_barrier_sync(1, kThreads);  // every role is done with TMEM
-    if (warp == kMmaWarp) {
-      tc_fence_after();
-      tmem_dealloc(tmem, 512);
-    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   } else {
-    named_barrier_sync(1, kThreads);  // idle warp of the control warpgroup
+    named_barrier_sync(1, kThreads);  // the two idle warps of the control warpgroup
   }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
