@@ -87,6 +87,7 @@ struct Bars {
 struct Params {
   const int32_t* tiles;  // [ntiles][8]
   long long ntiles;
+  long long block_tiles;  // work-list tiles per block of units (see load_unit)
   int hq, hkv, group, npairs;
   float scale_log2;      // scale * log2(e)
   long long T;
@@ -107,10 +108,25 @@ struct Unit {
   int ntiles_kv;
 };
 
+// Units are taken in blocks of `block_tiles` consecutive work-list tiles
+// (grid / pairs per head, so one round of the persistent grid is one block);
+// inside a block the order is KV head, then tile, then query-head pair.  So the
+// CTAs of one round all stream the same head's K/V (the same key prefix, for
+// the tiles of one long document) at about the same time, and each K/V tile is
+// read from HBM about once per round instead of once per CTA.  Blocks follow
+// the heaviest-first order of the work list.
 __device__ __forceinline__ Unit load_unit(const Params& p, long long u) {
   const long long per_tile = static_cast<long long>(p.hkv) * p.npairs;
-  const long long ti = u / per_tile;
-  const int r = static_cast<int>(u - ti * per_tile);
+  const long long blk_units = p.block_tiles * per_tile;
+  const long long blk = u / blk_units;
+  const long long r0 = u - blk * blk_units;
+  const long long t0 = blk * p.block_tiles;
+  const long long gb = p.ntiles - t0 < p.block_tiles ? p.ntiles - t0 : p.block_tiles;  // tiles in this block
+  const long long per_head = gb * p.npairs;
+  const int kvh = static_cast<int>(r0 / per_head);
+  const long long rem = r0 - kvh * per_head;
+  const long long ti = t0 + rem / p.npairs;
+  const int r = kvh * p.npairs + static_cast<int>(rem - (rem / p.npairs) * p.npairs);
   const int4* row = reinterpret_cast<const int4*>(p.tiles + ti * 8);
   const int4 a = __ldg(row), b = __ldg(row + 1);
   Unit x;
@@ -689,6 +705,7 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   HDP_CUDA_TRY(cudaGetDevice(&dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int grid = static_cast<int>(units < sms ? units : sms);
+  prm.block_tiles = grid / prm.npairs > 0 ? grid / prm.npairs : 1;
   const int smem = SmemLayout<D>::kBytes + 1024;
   HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   k_attn_fwd<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
