@@ -82,8 +82,8 @@ def attn_kernel_source_sha256() -> str:
 # to the value it was captured with.
 PROFILED_TRAFFIC = {
     ("seq128k", "fused"): {
-        "kernel_source_sha256": "779f5298ce1b6f52a2967c58174205afe6461b30402e05377e8b3e908c957f58",
-        "dram_bytes_per_launch": 173530875648 + 1083252736,
+        "kernel_source_sha256": "456a6a87ef651e2e095a7746d47985bcc70443fd006d2510eb20755c5e3349cb",
+        "dram_bytes_per_launch": 10955511552 + 1089511424,
         "source": "ncu capture summarised in profiles/attn_fwd_seq128k.md",
     },
 }
