@@ -11,9 +11,9 @@
 // Two persistent kernels (one CTA per SM, 12 warps), so that no partial sum
 // ever goes through global memory:
 //  - dK/dV pass: a work unit is one key tile (128 keys of one document) for
-//    one key/value head; it walks every query head of that head's GQA group
-//    and every query tile of the document from the key tile's diagonal on
-//    (fully masked tiles are never touched); dK and dV accumulate in TMEM.
+//    one key/value head; it walks every query tile of the document from the
+//    key tile's diagonal on, and for each every query head of that head's GQA
+//    group (fully masked tiles are never touched); dK and dV accumulate in TMEM.
 //  - dQ pass (further below): a unit is one query tile of one query head; it
 //    walks the causal key tiles; dQ accumulates in TMEM.
 // S and dP are computed by both passes (seven tile products instead of
@@ -106,6 +106,8 @@ struct BwdBars {
 struct BwdParams {
   const int32_t* tiles;  // fused work list [ntiles][8]; walked backwards
   long long ntiles;
+  long long block_kv;    // dK/dV pass: key tiles per block of units (see bwd_unit)
+  long long block_q;     // dQ pass: query tiles per block of units (see dq_unit)
   int hq, hkv, group;
   long long T;
   float scale, scale_log2;
@@ -121,8 +123,19 @@ struct BwdUnit {
   int k_row0, k_rows, doc_start, doc_len, j, n, kvh, iters;
 };
 
+// Units are taken in blocks of `block_kv` key tiles (a grid round covers
+// heads_per_round heads of a block), KV head major inside a block: with one
+// head per round (long documents) the CTAs of a round all walk the same
+// head's Q / dO tiles, from the document's last query tile down, at about the
+// same time, so each of those tiles is read from HBM about once per round.
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, long long u) {
-  const long long ti = u / p.hkv;
+  const long long blk_units = p.block_kv * p.hkv;
+  const long long blk = u / blk_units;
+  const long long r0 = u - blk * blk_units;
+  const long long t0 = blk * p.block_kv;
+  const long long gb = p.ntiles - t0 < p.block_kv ? p.ntiles - t0 : p.block_kv;  // key tiles in this block
+  const int kvh = static_cast<int>(r0 / gb);
+  const long long ti = t0 + (r0 - kvh * gb);
   const int4* row = reinterpret_cast<const int4*>(p.tiles + (p.ntiles - 1 - ti) * 8);
   const int4 a = __ldg(row), b = __ldg(row + 1);
   BwdUnit x;
@@ -132,16 +145,16 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, long long u) {
   x.doc_len = b.w;
   x.j = b.y / kTile;
   x.n = (x.doc_len + kTile - 1) / kTile;
-  x.kvh = static_cast<int>(u - ti * p.hkv);
+  x.kvh = kvh;
   x.iters = p.group * (x.n - x.j);
   return x;
 }
 
-// The iterations of a unit: for each query head of the GQA group in turn,
-// the query tiles from the document's last one down to the key tile's
-// diagonal.  Every unit of a document starts at the same tile, so the CTAs
-// working on one GQA group read the same Q / dO tiles at about the same time
-// and those stay in L2.
+// The iterations of a unit: the query tiles from the document's last one down
+// to the key tile's diagonal, and for each tile every query head of the GQA
+// group.  Every unit of a document starts at the same tile and the units of
+// one round share a KV head, so the CTAs of a round read the same Q / dO tiles
+// at about the same time and those stay in L2.
 __device__ __forceinline__ long long bwd_unit_index(long long k, int cta, int nctas) {
   return k * nctas + ((k & 1) ? (nctas - 1 - cta) : cta);
 }
@@ -261,11 +274,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ++qround;
           }
           q_armed = ++g;
-          if (i == x.j) {
-            i = x.n - 1;
-            ++h;
-          } else {
+          if (h == (x.kvh + 1) * p.group - 1) {
+            h = x.kvh * p.group;
             --i;
+          } else {
+            ++h;
           }
         }
       }
@@ -455,8 +468,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdUnit x = bwd_unit(p, u);
       const int key_local = x.j * kTile + r;
       const bool key_ok = key_local < x.doc_len;
-      // query tile i from n - 1 down to j, then the next head of the group
-      int i = x.n - 1;                               // this iteration's query tile
+      // query tile i from n - 1 down to j; for each, every head of the group
+      int i = x.n - 1, hi = 0;                       // this iteration's query tile and head in the group
       int nh = x.kvh * p.group, ni = x.n - 1;        // the tile `pre` is loaded for
       // Staging: -LSE log2(e) and -D scale (the addends of the FMAs below)
       // of a tile's queries are written once every warp is done with the
@@ -522,11 +535,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
         // the next tile's LSE / D: it has a whole tile to land
-        if (ni == x.j) {
-          ni = x.n - 1;
-          ++nh;
-        } else {
+        if (nh == (x.kvh + 1) * p.group - 1) {
+          nh = x.kvh * p.group;
           --ni;
+        } else {
+          ++nh;
         }
         if (it + 1 < x.iters) pre = staged(x, nh, ni);
         // ---- dS phase
@@ -571,7 +584,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dl_s[t] = pre * mult;
           named_barrier_or(kDsBarrier, 256, false);
         }
-        i = i == x.j ? x.n - 1 : i - 1;
+        if (++hi == p.group) {
+          hi = 0;
+          --i;
+        }
         ++g;
       }
       // a failed dP wait in the unit's last tile is seen by every warp here
@@ -655,8 +671,20 @@ struct DqUnit {
   int q_row0, q_rows, doc_start, doc_len, i, ntk, h, kvh;
 };
 
+// Units in blocks of `block_q` query tiles (a grid round covers
+// heads_per_round heads of a block), KV head major inside a block (then tile,
+// then query head of the group): with one head per round the CTAs of a round
+// stream the same head's K / V tiles together, for L2 reuse.
 __device__ __forceinline__ DqUnit dq_unit(const BwdParams& p, long long u) {
-  const long long ti = u / p.hq;
+  const long long blk_units = p.block_q * p.hq;
+  const long long blk = u / blk_units;
+  const long long r0 = u - blk * blk_units;
+  const long long t0 = blk * p.block_q;
+  const long long gb = p.ntiles - t0 < p.block_q ? p.ntiles - t0 : p.block_q;  // query tiles in this block
+  const long long per_head = gb * p.group;
+  const int kvh = static_cast<int>(r0 / per_head);
+  const long long rem = r0 - kvh * per_head;
+  const long long ti = t0 + rem / p.group;
   const int4* row = reinterpret_cast<const int4*>(p.tiles + ti * 8);
   const int4 a = __ldg(row), b = __ldg(row + 1);
   DqUnit x;
@@ -666,8 +694,8 @@ __device__ __forceinline__ DqUnit dq_unit(const BwdParams& p, long long u) {
   x.ntk = (a.w + kTile - 1) / kTile;  // key tiles of the causal range
   x.i = b.y / kTile;
   x.doc_len = b.w;
-  x.h = static_cast<int>(u - ti * p.hq);
-  x.kvh = x.h / p.group;
+  x.h = kvh * p.group + static_cast<int>(rem - (rem / p.group) * p.group);
+  x.kvh = kvh;
   return x;
 }
 
@@ -1073,6 +1101,8 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   {
     const long long units = prm.ntiles * hkv;
     const int grid = static_cast<int>(units < sms ? units : sms);
+    const long long bk = grid / heads_per_round(plan->v.max_doc_len, hkv);
+    prm.block_kv = bk > 0 ? bk : 1;
     const int smem = BwdSmem<D>::kBytes + 1024;
     HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     k_attn_bwd<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);
@@ -1083,6 +1113,8 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   {
     const long long units = prm.ntiles * hq;
     const int grid = static_cast<int>(units < sms ? units : sms);
+    const long long bq = grid / (prm.group * heads_per_round(plan->v.max_doc_len, hkv));
+    prm.block_q = bq > 0 ? bq : 1;
     const int smem = DqSmem<D>::kBytes + 1024;
     HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     k_attn_bwd_dq<D><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, prm);

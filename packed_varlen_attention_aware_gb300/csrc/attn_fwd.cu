@@ -109,12 +109,13 @@ struct Unit {
 };
 
 // Units are taken in blocks of `block_tiles` consecutive work-list tiles
-// (grid / pairs per head, so one round of the persistent grid is one block);
-// inside a block the order is KV head, then tile, then query-head pair.  So the
-// CTAs of one round all stream the same head's K/V (the same key prefix, for
-// the tiles of one long document) at about the same time, and each K/V tile is
-// read from HBM about once per round instead of once per CTA.  Blocks follow
-// the heaviest-first order of the work list.
+// (grid / (pairs per head x heads per round), so a round of the persistent
+// grid covers `heads_per_round` heads of one block); inside a block the order
+// is KV head, then tile, then query-head pair.  With one head per round (long
+// documents) the CTAs of a round all stream the same head's K/V (the same key
+// prefix, for the tiles of one long document) at about the same time, and
+// each K/V tile is read from HBM about once per round instead of once per
+// CTA.  Blocks follow the heaviest-first order of the work list.
 __device__ __forceinline__ Unit load_unit(const Params& p, long long u) {
   const long long per_tile = static_cast<long long>(p.hkv) * p.npairs;
   const long long blk_units = p.block_tiles * per_tile;
@@ -705,7 +706,8 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   HDP_CUDA_TRY(cudaGetDevice(&dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int grid = static_cast<int>(units < sms ? units : sms);
-  prm.block_tiles = grid / prm.npairs > 0 ? grid / prm.npairs : 1;
+  const long long bt = grid / (prm.npairs * heads_per_round(plan->v.max_doc_len, hkv));
+  prm.block_tiles = bt > 0 ? bt : 1;
   const int smem = SmemLayout<D>::kBytes + 1024;
   HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   k_attn_fwd<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);

@@ -21,6 +21,14 @@ hdp_status_t fail_cuda(cudaError_t e, const char* what);
     if (e_ != cudaSuccess) return ::hdp::fail_cuda(e_, #expr); \
   } while (0)
 
+// KV heads whose units share one round of a persistent attention grid.  One
+// head per round makes the CTAs of a round stream the same head's tiles at
+// about the same time (L2 reuse), which pays on long documents, whose causal
+// prefixes outgrow the L2; with many short documents it would put units of
+// very different sizes into one round, so every head takes part in each round
+// there.  `max_doc_len` is the plan's longest document.
+inline int heads_per_round(long long max_doc_len, int hkv) { return max_doc_len >= 65536 ? 1 : hkv; }
+
 // Device error word shared by all kernels (bounded-wait timeouts, internal
 // consistency checks).  Defined in api.cu; read by hdp_device_status.
 unsigned int* device_error_word();
