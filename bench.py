@@ -412,8 +412,11 @@ def our_arm(args, ws, rank, local):
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     attn_events = []
 
+    # a FUSED step needs no SPLIT work list
+    plan_flags = pkg.HDP_PLAN_NO_SPLIT if mode == pkg.HDP_MODE_FUSED else pkg.HDP_PLAN_DEFAULT
+
     def step(record=False):
-        plan = pkg.hdp_plan_create(lengths_d, w.capacity, stream=stream)
+        plan = pkg.hdp_plan_create(lengths_d, w.capacity, flags=plan_flags, stream=stream)
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -495,7 +498,7 @@ def our_arm(args, ws, rank, local):
     def compute_and_download(i):
         b = i & 1
         stream.wait_event(ev_in[b])
-        plan = pkg.hdp_plan_create(ld[b], w.capacity, stream=stream)
+        plan = pkg.hdp_plan_create(ld[b], w.capacity, flags=plan_flags, stream=stream)
         pkg.hdp_attention_fwd(plan, qd[b], kd[b], vd[b], w.hq, w.hkv, w.d, w.scale, mode, workspace, od[b], lsed[b],
                               stream=stream)
         pkg.hdp_flops_per_shard(plan, w.d, w.hq, fd[b], stream=stream)

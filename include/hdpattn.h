@@ -63,6 +63,10 @@ typedef enum {
 #define HDP_PLAN_NO_SHARDS 1u /* skip best-fit shard packing (num_shards = 0,
                                  shard_of_chunk = NULL); for callers that only
                                  need the attention tables */
+#define HDP_PLAN_NO_SPLIT 2u  /* skip the SPLIT work list (num_tiles_split = 0,
+                                 tiles_split = NULL); for callers that run FUSED
+                                 only.  SPLIT attention on such a plan fails
+                                 with INVALID_ARGUMENT */
 
 typedef struct hdp_plan_s* hdp_plan_t;
 
@@ -111,7 +115,8 @@ typedef struct {
  * ties, else a new shard), and build the query-tile work lists.
  *   d_lengths  [num_docs] int32 device array, every entry >= 1.
  *   num_docs   >= 1.      capacity >= 1.
- *   flags      HDP_PLAN_DEFAULT or HDP_PLAN_NO_SHARDS.
+ *   flags      HDP_PLAN_DEFAULT, or HDP_PLAN_NO_SHARDS and / or
+ *              HDP_PLAN_NO_SPLIT OR-ed together.
  *   out        receives the plan (NULL on failure).
  * Blocks the host once, to read the totals and the shard count back (best fit
  * runs on the device before that read-back).  Fails with INVALID_ARGUMENT for a

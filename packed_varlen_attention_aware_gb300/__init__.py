@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     HDP_OK,
     HDP_PLAN_DEFAULT,
     HDP_PLAN_NO_SHARDS,
+    HDP_PLAN_NO_SPLIT,
     HdpError,
     OffloadModel,
     Plan,

@@ -23,6 +23,7 @@ HDP_MODE_FUSED = 0
 HDP_MODE_SPLIT = 1
 HDP_PLAN_DEFAULT = 0
 HDP_PLAN_NO_SHARDS = 1
+HDP_PLAN_NO_SPLIT = 2
 HDP_BALANCE_DP = 0
 HDP_BALANCE_PP = 1
 

@@ -759,6 +759,8 @@ extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const 
   float* o_part = nullptr;
   float* lse_part = nullptr;
   if (split) {
+    if (plan->flags & HDP_PLAN_NO_SPLIT)
+      return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT on a plan created with HDP_PLAN_NO_SPLIT");
     if (plan->v.capacity % kTile != 0 || !plan->v.tiles_split)
       return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT needs capacity % 128 == 0");
     size_t ob = 0, need = 0;

@@ -654,9 +654,11 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   if (!d_lengths) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: d_lengths is NULL");
   if (num_docs < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: num_docs must be >= 1");
   if (capacity < 1) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: capacity must be >= 1");
-  if (flags & ~HDP_PLAN_NO_SHARDS) return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: unknown flags");
+  if (flags & ~(HDP_PLAN_NO_SHARDS | HDP_PLAN_NO_SPLIT))
+    return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_plan_create: unknown flags");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool split_ok = capacity % kTile == 0;
+  const bool split_list = split_ok && !(flags & HDP_PLAN_NO_SPLIT);  // build the SPLIT work list
   const int32_t n = num_docs;
   const int nblk = static_cast<int>((static_cast<long long>(n) + kScanTile - 1) / kScanTile);
 
@@ -758,7 +760,7 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   const size_t o_cp = off; off = align256(off + sizeof(int64_t) * nc);
   const size_t o_sc = off; off = align256(off + (shards ? sizeof(int32_t) * nc : 0));
   const size_t o_tf = off; off = align256(off + sizeof(int32_t) * 8 * ntf);
-  const size_t o_ts = off; off = align256(off + sizeof(int32_t) * 8 * nts);
+  const size_t o_ts = off; off = align256(off + (split_list ? sizeof(int32_t) * 8 * nts : 0));
   const size_t bytes2 = off;
   e = cudaMallocAsync(&plan->mem, bytes2, st);
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan tables)"));
@@ -768,12 +770,12 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   int64_t* chunk_pairs = reinterpret_cast<int64_t*>(m2 + o_cp);
   int32_t* shard_of_chunk = shards ? reinterpret_cast<int32_t*>(m2 + o_sc) : nullptr;
   int32_t* tiles_f = reinterpret_cast<int32_t*>(m2 + o_tf);
-  int32_t* tiles_s = split_ok ? reinterpret_cast<int32_t*>(m2 + o_ts) : nullptr;
+  int32_t* tiles_s = split_list ? reinterpret_cast<int32_t*>(m2 + o_ts) : nullptr;
 
   // sort scratch: keys (power of two) + unsorted rows
-  const long long sort_n = std::max({ntf, split_ok ? nts : 0ll, 2ll});
+  const long long sort_n = std::max({ntf, split_list ? nts : 0ll, 2ll});
   const long long n2 = next_pow2(sort_n);
-  const long long nrows = std::max(ntf, split_ok ? nts : 0ll);
+  const long long nrows = std::max(ntf, split_list ? nts : 0ll);
   char* sort_mem = nullptr;
   const size_t o_keys = 0;
   size_t so = align256(sizeof(unsigned long long) * n2);
@@ -804,7 +806,7 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   k_gather_rows<<<grid_for(ntf, 256), 256, 0, st>>>(keys, ntf, rows, tiles_f);
   note_launch();
   // split work list
-  if (split_ok && nts > 0) {
+  if (split_list && nts > 0) {
     k_fill_tiles_split<<<grid_for(nts, 256), 256, 0, st>>>(n, capacity, nts, cu, bo, tos, rows, keys);
     note_launch();
     e = sort_keys(keys, nts, st);
@@ -836,7 +838,7 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   plan->v.tiles_fused = tiles_f;
   plan->v.num_tiles_fused = ntf;
   plan->v.tiles_split = tiles_s;
-  plan->v.num_tiles_split = split_ok ? nts : 0;
+  plan->v.num_tiles_split = split_list ? nts : 0;
   plan->tile_offsets_fused = tof;
   plan->tile_offsets_split = tos;
   plan->mem1 = mem1;

@@ -12,7 +12,7 @@ import oracle
 import packed_varlen_attention_aware_gb300 as pkg
 from packed_varlen_attention_aware_gb300 import workloads as wl
 
-from parity_util import check_plan, full_parity, run_gpu, sample_rows, sampled_parity
+from parity_util import PLAN_KEYS, check_plan, full_parity, run_gpu, sample_rows, sampled_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +74,36 @@ def test_plan_create_blocks_the_host_once():
             pkg.hdp_flops_per_shard(plan, w.d, w.hq, f)
             assert pkg.hdp_host_sync_count() - n0 == 1
         plan.destroy()
+
+
+def test_plan_without_split_list():
+    """HDP_PLAN_NO_SPLIT leaves out the SPLIT work list only: every other table
+    is the default plan's, FUSED attention still runs, SPLIT is refused."""
+    lengths = [700, 130, 5, 1024, 77]
+    dl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    ref = oracle.plan(lengths, 256)
+    for flags in (pkg.HDP_PLAN_NO_SPLIT, pkg.HDP_PLAN_NO_SPLIT | pkg.HDP_PLAN_NO_SHARDS):
+        with pkg.hdp_plan_create(dl, 256) as full, pkg.hdp_plan_create(dl, 256, flags=flags) as plan:
+            a, b = full.tables(), plan.tables()
+            assert plan.view.num_tiles_split == 0 and "tiles_split" not in b
+            for key in PLAN_KEYS + ("tiles_fused",):
+                assert np.array_equal(a[key], b[key]), key
+            assert np.array_equal(b["tiles_fused"], oracle.tile_worklist(ref, 128, split=False))
+            w = wl.Workload("case", tuple(lengths), 256, 4, 2, 64, 1.0, 3)
+            q, k, v = wl.qkv(w, device="cuda")
+            o, lse = torch.empty_like(q), torch.empty(w.hq, sum(lengths), dtype=torch.float32, device="cuda")
+            o2, lse2 = torch.empty_like(q), torch.empty_like(lse)
+            pkg.hdp_attention_fwd(full, q, k, v, w.hq, w.hkv, w.d, w.scale, FUSED, None, o, lse)
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, FUSED, None, o2, lse2)
+            assert torch.equal(o, o2) and torch.equal(lse, lse2)
+            ws = torch.empty(pkg.hdp_attention_workspace_bytes(full, w.hq, w.d, SPLIT), dtype=torch.uint8,
+                             device="cuda")
+            with pytest.raises(pkg.HdpError) as e:
+                pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, SPLIT, ws, o2, lse2)
+            assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
+    with pytest.raises(pkg.HdpError) as e:
+        pkg.hdp_plan_create(dl, 256, flags=4)
+    assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
 
 
 def test_plan_rejects_too_many_pieces_for_best_fit():
