@@ -12,7 +12,7 @@ import oracle
 import packed_varlen_attention_aware_gb300 as pkg
 from packed_varlen_attention_aware_gb300 import workloads as wl
 
-from parity_util import PLAN_KEYS, check_plan, full_parity, run_gpu, sample_rows, sampled_parity
+from parity_util import PLAN_KEYS, check_plan, compare, full_parity, run_gpu, sample_rows, sampled_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -191,6 +191,91 @@ def test_merge_rows_against_oracle():
     assert got_l[0] == -np.inf and np.all(got_o[0] == 0)
     assert np.max(np.abs(got_o[1:] - o_ref[1:])) <= 1.6e-2
     assert np.max(np.abs(got_l[1:] - lse_ref[1:])) <= 1e-5
+
+
+# ---------------------------------------------------------------- degenerate and extreme inputs
+
+def _scaled_parity(q, k, v, lengths, hq, hkv, d, C, mode, scale):
+    o, lse, plan = run_gpu(q.cuda(), k.cuda(), v.cuda(), lengths, C, mode)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    o_ref, lse_ref = oracle.attention(wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v), cu, hq, hkv, d, scale)
+    compare(o.double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, lse_ref, f"{lengths} mode={mode}")
+    plan.destroy()
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_rising_scores_take_the_rescale_path_every_tile(mode):
+    """Scores that rise by ~12 in the exp2 domain from one key tile to the
+    next: every steady tile's maximum exceeds the stale running maximum by
+    more than 2^8, so the softmax recomputes the tile and rescales O each time.
+    The logits reach ~100 nats, far outside exp's fp32 range without the
+    running maximum."""
+    lengths, hq, hkv, d, C = [1500, 700, 129], 8, 2, 128, 256
+    w = wl.Workload("case", tuple(lengths), C, hq, hkv, d, 1.0, 21)
+    q, k, v = wl.qkv(w, device="cpu")
+    q[:, :, 0] = 8.0
+    start = 0
+    for s in lengths:
+        tile = torch.arange(s) // 128
+        k[start:start + s, :, 0] = (12.0 * tile).to(torch.bfloat16)[:, None]
+        start += s
+    _scaled_parity(q, k, v, lengths, hq, hkv, d, C, mode, w.scale)
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_large_random_logits(mode):
+    """Q and K with standard deviation 4: scores of standard deviation 16
+    nats, so the running maximum often grows past the rescale threshold at
+    random places, and most rows put nearly all their weight on a few keys.
+
+    Such inputs lie outside the five workloads the pages' tolerance is stated
+    for, so the bound on max|dO| comes from the arithmetic instead: o = sum_j
+    P_j v_j / l with every P_j rounded to bf16 before the P.V product (relative
+    error <= 2^-8, the unit roundoff of 8 significant bits) and l summed from
+    the unrounded P_j, then o rounded to bf16 (<= 2^-8 |o|).  Per row that is
+    at most 2^-8 max_j |v_j| + 2^-8 |o| <= 2^-7 max|v|.  Spread-out rows (the
+    workloads') average those roundings away; a row on one or two keys does
+    not.  The mean and LSE bars are the pages' own."""
+    lengths, hq, hkv, d, C = [1100, 333, 2], 4, 2, 128, 384
+    w = wl.Workload("case", tuple(lengths), C, hq, hkv, d, 1.0, 22)
+    q, k, v = wl.qkv(w, device="cpu")
+    q = (q.float() * 4).to(torch.bfloat16)
+    k = (k.float() * 4).to(torch.bfloat16)
+    o, lse, plan = run_gpu(q.cuda(), k.cuda(), v.cuda(), lengths, C, mode)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    o_ref, lse_ref = oracle.attention(wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v), cu, hq, hkv, d, w.scale)
+    plan.destroy()
+    do = np.abs(o.double().cpu().numpy() - o_ref)
+    dl = np.abs(lse.double().cpu().numpy() - lse_ref)
+    bound = 2.0 ** -7 * float(v.float().abs().max())
+    msg = f"max|dO|={do.max():.3e} (bound {bound:.3e}) mean|dO|={do.mean():.3e} max|dLSE|={dl.max():.3e}"
+    assert do.max() <= bound, msg
+    assert do.mean() <= 1e-3, msg
+    assert dl.max() <= 2e-3, msg
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_many_tiny_documents(mode):
+    """400 documents of 1 to 40 tokens packed together: many units, most query
+    tiles straddle several documents' boundaries."""
+    rng = np.random.default_rng(7)
+    lengths = [int(x) for x in rng.integers(1, 41, 400)]
+    full_parity(lengths, 4, 1, 64, 128, mode, seed=11)
+
+
+def test_capacity_not_a_tile_multiple():
+    """FUSED does not depend on C; SPLIT's blocks must be whole tiles, so a
+    capacity that is not a multiple of 128 is refused for it."""
+    lengths = [500, 77, 1, 260]
+    full_parity(lengths, 4, 2, 128, 100, FUSED, seed=5)
+    w = wl.Workload("case", tuple(lengths), 100, 4, 2, 128, 1.0, 5)
+    q, k, v = wl.qkv(w, device="cuda")
+    dl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    o, lse = torch.empty_like(q), torch.empty(4, sum(lengths), dtype=torch.float32, device="cuda")
+    with pkg.hdp_plan_create(dl, 100) as plan:
+        with pytest.raises(pkg.HdpError) as e:
+            pkg.hdp_attention_fwd(plan, q, k, v, 4, 2, 128, w.scale, SPLIT, None, o, lse)
+        assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
 
 
 # ---------------------------------------------------------------- named workloads, sampled rows
