@@ -175,8 +175,8 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
  *     64 MiB are rejected with HDP_ERR_INVALID_ARGUMENT and a message.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
  *     call on a device resolves the scratch array's device address (once per
- *     device, with that device current) and caches it; make that first call
- *     before any stream capture.  A cudaDeviceReset, or anything else that
+ *     device, with that device current) and caches it.  A cudaDeviceReset, or
+ *     anything else that
  *     destroys the device's primary context, invalidates the cached address
  *     (and the device error word's): do not call the library on that device
  *     after such a reset in the same process.
