@@ -175,11 +175,10 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
  *     64 MiB are rejected with HDP_ERR_INVALID_ARGUMENT and a message.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
  *     call on a device resolves the scratch array's device address (once per
- *     device, with that device current) and caches it.  A cudaDeviceReset, or
- *     anything else that
- *     destroys the device's primary context, invalidates the cached address
- *     (and the device error word's): do not call the library on that device
- *     after such a reset in the same process.
+ *     device, with that device current) and caches it.  A cudaDeviceReset,
+ *     or anything else that destroys the device's primary context,
+ *     invalidates the cached address (and the device error word's): do not
+ *     call the library on that device after such a reset in the same process.
  *   - Every call shares the one scratch array, which keeps the last call's
  *     contents; every partial a call reads is written by that call first, so
  *     nothing needs to start at zero.  Calls that overlap on the GPU (other
