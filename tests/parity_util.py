@@ -2,6 +2,8 @@
 C ABI, run the fp64 oracle on the same bytes, compare within the tolerances."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -52,10 +54,18 @@ def run_gpu(q, k, v, lengths, C, mode, plan=None):
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """o_gpu/lse_gpu: float64 numpy arrays of the CUDA results (same shape as refs)."""
+    """o_gpu/lse_gpu: float64 numpy arrays of the CUDA results (same shape as refs).
+
+    The message also counts the reference elements with |O| >= 4, where half
+    a bf16 ulp (2^-6 = 0.0156) alone exceeds the 1.5e-2 bar: rows with very
+    few keys, where O is about one v value."""
     do = np.abs(o_gpu - o_ref)
     dl = np.abs(lse_gpu - lse_ref)
-    msg = f"{what}: max|dO|={do.max():.3e} mean|dO|={do.mean():.3e} max|dLSE|={dl.max():.3e}"
+    big = int(np.count_nonzero(np.abs(o_ref) >= 4.0))
+    msg = (f"{what}: max|dO|={do.max():.3e} mean|dO|={do.mean():.3e} max|dLSE|={dl.max():.3e} "
+           f"|O|>=4: {big} of {o_ref.size}")
+    if os.environ.get("HDP_PARITY_REPORT"):
+        print("parity", msg, flush=True)
     assert np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all(), msg
     assert do.max() <= TOL_MAX_O, msg
     assert do.mean() <= TOL_MEAN_O, msg
