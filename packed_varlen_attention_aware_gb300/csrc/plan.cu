@@ -12,8 +12,9 @@
 //   k_fill_chunks / k_fill_blocks / k_fill_tiles_*
 //       one thread per table row; the row's document is found by binary
 //       search over the scanned offsets, the rest is closed-form.
-//   k_bitonic_*   sort of 64-bit keys (work lists heaviest first, pieces in
-//                 best-fit-decreasing order).
+//   k_radix_*     stable LSD radix sort of 32-bit keys with their indices,
+//                 8 bits a pass over the bits the largest key needs (work
+//                 lists heaviest first, pieces in best-fit-decreasing order).
 //   k_shard_bfd   one CTA: sequential best fit over the sorted pieces with a
 //                 block-wide argmin over the open shards.
 //   k_flops_*     exact int64 per-shard FLOPs.
@@ -33,9 +34,6 @@ constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;  // documents per CTA
 constexpr int kQ = 6;  // tokens, chunks, blocks, fused tiles, split tiles, pieces
 constexpr int kPartial = 8;  // kQ sums + max length + invalid-length flag
-constexpr int kIdxBits = 40;
-constexpr unsigned long long kIdxMask = (1ull << kIdxBits) - 1;
-constexpr long long kWeightCap = 1ll << 24;  // > max tiles of a document (2^31 / 128)
 
 // Per-document quantities (s >= 1).  32-bit unsigned division: every
 // intermediate is below 2^31 for s, C < 2^31.
@@ -341,10 +339,6 @@ __global__ void k_fill_blocks(int32_t n, long long nb, const int32_t* __restrict
   }
 }
 
-__device__ __forceinline__ unsigned long long tile_key(long long weight, long long idx) {
-  return (static_cast<unsigned long long>(kWeightCap - weight) << kIdxBits) | static_cast<unsigned long long>(idx);
-}
-
 __device__ __forceinline__ void store_tile(int32_t* out, long long t, int32_t q0, int32_t qrows, int32_t kv0,
                                            int32_t kvlen, int32_t blk, int32_t row_off, int32_t w, int32_t doc_len) {
   int4* o = reinterpret_cast<int4*>(out + t * 8);
@@ -353,9 +347,10 @@ __device__ __forceinline__ void store_tile(int32_t* out, long long t, int32_t q0
 }
 
 // One row per document query tile: keys are the document's causal prefix.
+// Sort key: w_max - weight (w_max >= every weight), so heaviest sorts first.
 __global__ void k_fill_tiles_fused(int32_t n, long long ntiles, const int32_t* __restrict__ cu,
-                                   const int64_t* __restrict__ tof, int32_t* __restrict__ rows,
-                                   unsigned long long* __restrict__ keys) {
+                                   const int64_t* __restrict__ tof, int32_t w_max, int32_t* __restrict__ rows,
+                                   uint32_t* __restrict__ keys) {
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < ntiles;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int32_t doc = upper_doc(tof, n, t);
@@ -367,15 +362,16 @@ __global__ void k_fill_tiles_fused(int32_t n, long long ntiles, const int32_t* _
     store_tile(rows, t, static_cast<int32_t>(cu[doc] + qt * kTile), static_cast<int32_t>(qrows), cu[doc],
                static_cast<int32_t>(kvlen), -1, static_cast<int32_t>(qt * kTile), static_cast<int32_t>(w),
                static_cast<int32_t>(s));
-    keys[t] = tile_key(w, t);
+    keys[t] = static_cast<uint32_t>(w_max - w);
   }
 }
 
 // One row per query tile of every causal block (qc, kc); rows of a document
 // are ordered by block (qc, kc ascending), then query tile.  Needs C % 128 == 0.
+// Sort key: C / 128 - weight.
 __global__ void k_fill_tiles_split(int32_t n, int32_t C, long long ntiles, const int32_t* __restrict__ cu,
                                    const int64_t* __restrict__ bo, const int64_t* __restrict__ tos,
-                                   int32_t* __restrict__ rows, unsigned long long* __restrict__ keys) {
+                                   int32_t* __restrict__ rows, uint32_t* __restrict__ keys) {
   const long long tpc = C / kTile;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < ntiles;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -407,88 +403,148 @@ __global__ void k_fill_tiles_split(int32_t n, int32_t C, long long ntiles, const
                static_cast<int32_t>(cu[doc] + kc * C), static_cast<int32_t>(kvlen),
                static_cast<int32_t>(bo[doc] + blk_local), static_cast<int32_t>(qt * kTile),
                static_cast<int32_t>(w), 0);
-    keys[t] = tile_key(w, t);
+    keys[t] = static_cast<uint32_t>(tpc - w);
   }
 }
 
-__global__ void k_fill_pad(unsigned long long* keys, long long from, long long to) {
-  for (long long i = from + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < to;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    keys[i] = ~0ull;
-}
+// ---------------------------------------------------------------- radix sort
+// Stable LSD radix sort of (32-bit key, index) pairs by key ascending, 8 bits a
+// pass over only the bits the largest key needs.  A pass is three launches:
+// block histograms, a scan per digit over the blocks, and a scatter that
+// places each block's items in index order (so equal keys keep their order).
+// The work lists sort by (largest weight - weight), the best-fit pieces by
+// (C - piece length): heaviest / longest first, then index ascending.
+constexpr int kRadixThreads = 256;  // also the number of digit values
+constexpr int kRadixItems = 8;      // items per thread per block
+constexpr int kRadixTile = kRadixThreads * kRadixItems;
+constexpr int kRadixWarps = kRadixThreads / 32;
 
-// ---------------------------------------------------------------- bitonic sort
-constexpr int kSortTile = 4096;
-constexpr int kSortThreads = 1024;
-
-__device__ __forceinline__ void cmp_swap(unsigned long long& a, unsigned long long& b, bool ascending) {
-  if ((a > b) == ascending) {
-    const unsigned long long t = a;
-    a = b;
-    b = t;
-  }
-}
-
-// Sorts each kSortTile segment for every stage k <= kSortTile (direction by
-// the global index), i.e. the first log2(kSortTile) merge levels.
-__global__ void __launch_bounds__(kSortThreads) k_bitonic_local(unsigned long long* keys, long long n2) {
-  __shared__ unsigned long long s[kSortTile];
-  const long long base = static_cast<long long>(blockIdx.x) * kSortTile;
-  const int len = static_cast<int>(n2 - base < kSortTile ? n2 - base : kSortTile);
-  for (int i = threadIdx.x; i < len; i += kSortThreads) s[i] = keys[base + i];
+// counts[d * nb + b] = items of block b whose digit is d.
+__global__ void __launch_bounds__(kRadixThreads) k_radix_hist(const uint32_t* __restrict__ keys, long long n,
+                                                              int shift, uint32_t* __restrict__ counts, int nb) {
+  __shared__ uint32_t h[kRadixThreads];
+  h[threadIdx.x] = 0;
   __syncthreads();
-  for (int k = 2; k <= len; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < len / 2; i += kSortThreads) {
-        const int lo = (i / j) * 2 * j + (i % j);
-        const int hi = lo + j;
-        const bool asc = ((base + lo) & k) == 0;
-        cmp_swap(s[lo], s[hi], asc);
+  const long long base = static_cast<long long>(blockIdx.x) * kRadixTile;
+#pragma unroll
+  for (int j = 0; j < kRadixItems; ++j) {
+    const long long i = base + j * kRadixThreads + threadIdx.x;
+    if (i < n) atomicAdd(&h[(keys[i] >> shift) & 255u], 1u);
+  }
+  __syncthreads();
+  counts[static_cast<long long>(threadIdx.x) * nb + blockIdx.x] = h[threadIdx.x];
+}
+
+// One CTA per digit: exclusive scan of its row of counts over the blocks, in
+// place; totals[d] = the digit's count.
+constexpr int kDigitScanThreads = 1024;
+__global__ void __launch_bounds__(kDigitScanThreads) k_radix_digit_scan(uint32_t* __restrict__ counts, int nb,
+                                                                        uint32_t* __restrict__ totals) {
+  __shared__ uint32_t wsum[kDigitScanThreads / 32];
+  __shared__ uint32_t carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* row = counts + static_cast<long long>(blockIdx.x) * nb;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < nb; b0 += kDigitScanThreads) {
+    const int i = b0 + threadIdx.x;
+    const uint32_t x = i < nb ? row[i] : 0u;
+    uint32_t v = x;  // inclusive scan inside the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t w = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
       }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < len; i += kSortThreads) keys[base + i] = s[i];
-}
-
-// One compare-exchange level with distance j >= kSortTile/2 of merge stage k.
-__global__ void k_bitonic_global(unsigned long long* keys, long long n2, long long k, long long j) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n2 / 2;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long lo = (i / j) * 2 * j + (i % j);
-    const long long hi = lo + j;
-    const bool asc = (lo & k) == 0;
-    unsigned long long a = keys[lo], b = keys[hi];
-    if ((a > b) == asc) {
-      keys[lo] = b;
-      keys[hi] = a;
-    }
-  }
-}
-
-// The remaining levels j < kSortTile/2 of merge stage k, inside one tile.
-__global__ void __launch_bounds__(kSortThreads) k_bitonic_tail(unsigned long long* keys, long long k) {
-  __shared__ unsigned long long s[kSortTile];
-  const long long base = static_cast<long long>(blockIdx.x) * kSortTile;
-  for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) s[i] = keys[base + i];
-  __syncthreads();
-  for (int j = kSortTile / 2; j > 0; j >>= 1) {
-    for (int i = threadIdx.x; i < kSortTile / 2; i += kSortThreads) {
-      const int lo = (i / j) * 2 * j + (i % j);
-      const int hi = lo + j;
-      const bool asc = ((base + lo) & k) == 0;
-      cmp_swap(s[lo], s[hi], asc);
+      wsum[lane] = w;
     }
     __syncthreads();
+    const uint32_t before = carry + (warp > 0 ? wsum[warp - 1] : 0u);
+    if (i < nb) row[i] = before + v - x;
+    __syncthreads();  // every thread has read carry
+    if (threadIdx.x == kDigitScanThreads - 1) carry = before + v;
+    __syncthreads();
   }
-  for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) keys[base + i] = s[i];
+  if (threadIdx.x == 0) totals[blockIdx.x] = carry;
 }
 
-__global__ void k_gather_rows(const unsigned long long* __restrict__ keys, long long count,
-                              const int32_t* __restrict__ rows, int32_t* __restrict__ out) {
+// Places every item of block b at digit_base[d] + counts[d][b] + (its rank
+// among the block's items with digit d, in index order).  vals_in == nullptr:
+// the value is the item's index (first pass).
+__global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const uint32_t* __restrict__ keys_in,
+                                                                 const uint32_t* __restrict__ vals_in,
+                                                                 uint32_t* __restrict__ keys_out,
+                                                                 uint32_t* __restrict__ vals_out, long long n,
+                                                                 int shift, const uint32_t* __restrict__ counts,
+                                                                 int nb, const uint32_t* __restrict__ totals) {
+  __shared__ uint32_t wcnt[kRadixWarps][kRadixThreads];  // per round: digit counts per warp, then offsets
+  __shared__ uint32_t base_d[kRadixThreads];             // where this block's items of digit d start
+  __shared__ uint32_t wsum[kRadixWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int d = threadIdx.x;  // one digit per thread for the per-digit steps
+  {
+    // exclusive scan of the digit totals -> start of each digit's output range
+    const uint32_t x = totals[d];
+    uint32_t v = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    base_d[d] = before + v - x + counts[static_cast<long long>(d) * nb + blockIdx.x];
+  }
+  const long long base = static_cast<long long>(blockIdx.x) * kRadixTile;
+  for (int j = 0; j < kRadixItems; ++j) {
+#pragma unroll
+    for (int e = lane; e < kRadixThreads; e += 32) wcnt[warp][e] = 0;
+    __syncthreads();  // (round 0: also orders base_d)
+    const long long i = base + j * kRadixThreads + threadIdx.x;
+    const bool valid = i < n;
+    const uint32_t key = valid ? keys_in[i] : 0u;
+    const uint32_t dig = valid ? (key >> shift) & 255u : 256u;  // 256: not an item
+    const uint32_t peers = __match_any_sync(0xffffffffu, dig);
+    const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) wcnt[warp][dig] = __popc(peers);
+    __syncthreads();
+    {
+      // per digit: items of earlier warps of this round, after earlier rounds
+      uint32_t off = base_d[d];
+#pragma unroll
+      for (int w = 0; w < kRadixWarps; ++w) {
+        const uint32_t c = wcnt[w][d];
+        wcnt[w][d] = off;
+        off += c;
+      }
+      base_d[d] = off;
+    }
+    __syncthreads();
+    if (valid) {
+      const uint32_t pos = wcnt[warp][dig] + rank;
+      keys_out[pos] = key;
+      vals_out[pos] = vals_in ? vals_in[i] : static_cast<uint32_t>(i);
+    }
+    __syncthreads();  // before the next round clears wcnt
+  }
+}
+
+// out row i = rows[perm[i]] (perm == nullptr: the identity).
+__global__ void k_gather_rows(const uint32_t* __restrict__ perm, long long count, const int32_t* __restrict__ rows,
+                              int32_t* __restrict__ out) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long src = static_cast<long long>(keys[i] & kIdxMask);
+    const long long src = perm ? static_cast<long long>(perm[i]) : i;
     const int4* a = reinterpret_cast<const int4*>(rows + src * 8);
     int4* b = reinterpret_cast<int4*>(out + i * 8);
     b[0] = a[0];
@@ -497,18 +553,17 @@ __global__ void k_gather_rows(const unsigned long long* __restrict__ keys, long 
 }
 
 // ---------------------------------------------------------------- best fit
-// Key of document i: its sub-capacity piece (short document or tail chunk) as
-// (C - len) << 32 | i, so ascending order is length descending, then document
-// ascending; documents without a piece (s a multiple of C, or an invalid
-// length) get ~0 and sort after every piece.
+// Sort key of document i: C - (length of its sub-capacity piece: a short
+// document or a tail chunk), so ascending order is length descending (then
+// document ascending, the sort being stable); documents without a piece (s a
+// multiple of C, or an invalid length) get C and sort after every piece.
 __global__ void k_piece_keys(int32_t n, int32_t C, const int32_t* __restrict__ lengths,
-                             unsigned long long* __restrict__ keys) {
+                             uint32_t* __restrict__ keys) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int32_t s = lengths[i];
     const int32_t last = s >= 1 ? s % C : 0;
-    keys[i] = last != 0 ? (static_cast<unsigned long long>(C - last) << 32) | static_cast<unsigned long long>(i)
-                        : ~0ull;
+    keys[i] = static_cast<uint32_t>(last != 0 ? C - last : C);
   }
 }
 
@@ -522,7 +577,8 @@ constexpr int kBfdThreads = 1024;
 // becomes the number of shards, or -1 when there are more than kMaxPieces
 // pieces (nothing else is written then).  piece_shard[doc] receives the shard
 // of the document's piece.
-__global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long long* __restrict__ keys, int32_t C,
+__global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const uint32_t* __restrict__ keys,
+                                                           const uint32_t* __restrict__ docs, int32_t C,
                                                            long long* __restrict__ totals,
                                                            int32_t* __restrict__ remaining,
                                                            int32_t* __restrict__ piece_shard) {
@@ -539,9 +595,8 @@ __global__ void __launch_bounds__(kBfdThreads) k_shard_bfd(const unsigned long l
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int32_t p = 0; p < npieces; ++p) {
-    const unsigned long long key = keys[p];
-    const int32_t len = C - static_cast<int32_t>(key >> 32);
-    const int32_t doc = static_cast<int32_t>(key & 0xffffffffu);
+    const int32_t len = C - static_cast<int32_t>(keys[p]);
+    const int32_t doc = docs ? static_cast<int32_t>(docs[p]) : p;
     const int32_t open = s_open;
     unsigned long long best = ~0ull;
     for (int32_t s = threadIdx.x; s < open; s += kBfdThreads) {
@@ -612,35 +667,70 @@ int grid_for(long long items, int threads, int cap = 1 << 16) {
   return static_cast<int>(g);
 }
 
-long long next_pow2(long long x) {
-  long long p = 1;
-  while (p < x) p <<= 1;
-  return p;
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int bit_length(uint32_t x) {
+  int b = 0;
+  while (x) {
+    ++b;
+    x >>= 1;
+  }
+  return b;
 }
 
-// Sort n keys in place (buffer holds next_pow2(max(n, 1)) entries, padded
-// here with ~0).
-cudaError_t sort_keys(unsigned long long* keys, long long n, cudaStream_t st) {
-  const long long n2 = next_pow2(n < 2 ? 2 : n);
-  if (n2 > n) {
-    k_fill_pad<<<grid_for(n2 - n, 256), 256, 0, st>>>(keys, n, n2);
+// Scratch of radix_sort for n items: two key and two value buffers of n
+// entries, the per-(digit, block) counts and the 256 digit totals.
+struct RadixScratch {
+  uint32_t *k0, *v0, *k1, *v1, *counts, *totals;
+};
+size_t radix_scratch_bytes(long long n) {
+  const long long nb = (n + kRadixTile - 1) / kRadixTile;
+  return 4 * align256(sizeof(uint32_t) * (n > 0 ? n : 1)) + align256(sizeof(uint32_t) * 256 * (nb > 0 ? nb : 1)) +
+         align256(sizeof(uint32_t) * 256);
+}
+RadixScratch radix_scratch(char* mem, long long n) {
+  const long long nb = (n + kRadixTile - 1) / kRadixTile;
+  const size_t a = align256(sizeof(uint32_t) * (n > 0 ? n : 1));
+  RadixScratch r;
+  r.k0 = reinterpret_cast<uint32_t*>(mem);
+  r.v0 = reinterpret_cast<uint32_t*>(mem + a);
+  r.k1 = reinterpret_cast<uint32_t*>(mem + 2 * a);
+  r.v1 = reinterpret_cast<uint32_t*>(mem + 3 * a);
+  r.counts = reinterpret_cast<uint32_t*>(mem + 4 * a);
+  r.totals = reinterpret_cast<uint32_t*>(mem + 4 * a + align256(sizeof(uint32_t) * 256 * (nb > 0 ? nb : 1)));
+  return r;
+}
+
+// Stable sort of the n keys in sc.k0 (every key <= max_key) with their
+// indices.  *keys / *perm receive the sorted keys and the source index of
+// each position (perm == nullptr when no pass was needed: the identity,
+// keys == sc.k0).
+cudaError_t radix_sort(RadixScratch sc, long long n, uint32_t max_key, cudaStream_t st, const uint32_t** keys,
+                       const uint32_t** perm) {
+  const int passes = (bit_length(max_key) + 7) / 8;
+  const int nb = static_cast<int>((n + kRadixTile - 1) / kRadixTile);
+  uint32_t *kin = sc.k0, *vin = nullptr, *kout = sc.k1, *vout = sc.v1;
+  for (int p = 0; p < passes && n > 0; ++p) {
+    const int shift = 8 * p;
+    k_radix_hist<<<nb, kRadixThreads, 0, st>>>(kin, n, shift, sc.counts, nb);
     note_launch();
-  }
-  const long long tiles = (n2 + kSortTile - 1) / kSortTile;
-  k_bitonic_local<<<static_cast<unsigned>(tiles), kSortThreads, 0, st>>>(keys, n2);
-  note_launch();
-  for (long long k = 2LL * kSortTile; k <= n2; k <<= 1) {
-    for (long long j = k >> 1; j >= kSortTile; j >>= 1) {
-      k_bitonic_global<<<grid_for(n2 / 2, 256), 256, 0, st>>>(keys, n2, k, j);
-      note_launch();
-    }
-    k_bitonic_tail<<<static_cast<unsigned>(n2 / kSortTile), kSortThreads, 0, st>>>(keys, k);
+    k_radix_digit_scan<<<256, kDigitScanThreads, 0, st>>>(sc.counts, nb, sc.totals);
     note_launch();
+    k_radix_scatter<<<nb, kRadixThreads, 0, st>>>(kin, vin, kout, vout, n, shift, sc.counts, nb, sc.totals);
+    note_launch();
+    // this pass's output is the next pass's input; its input buffers are free
+    uint32_t* const free_k = kin;
+    uint32_t* const free_v = vin ? vin : sc.v0;
+    kin = kout;
+    vin = vout;
+    kout = free_k;
+    vout = free_v;
   }
+  *keys = kin;
+  *perm = vin;
   return cudaGetLastError();
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 }  // namespace hdp
@@ -667,7 +757,6 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   // the best-fit state and the per-document piece shards are sized by n and
   // run before the one host read-back, which then carries the shard count.
   const bool shards = !(flags & HDP_PLAN_NO_SHARDS);
-  const long long n2p = shards ? next_pow2(n < 2 ? 2 : n) : 0;
   size_t off = 0;
   const size_t o_cu = off; off = align256(off + sizeof(int32_t) * (n + 1));
   const size_t o_co = off; off = align256(off + sizeof(int32_t) * (n + 1));
@@ -679,7 +768,7 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   size_t soff = align256(sizeof(int32_t) * (n + 1));
   const size_t o_part = soff; soff = align256(soff + sizeof(long long) * kPartial * nblk);
   const size_t o_tot = soff; soff = align256(soff + sizeof(long long) * (kPartial + 1));
-  const size_t o_pkey = soff; soff = align256(soff + sizeof(unsigned long long) * n2p);
+  const size_t o_pkey = soff; soff = align256(soff + (shards ? radix_scratch_bytes(n) : 0));
   const size_t o_rem = soff; soff = align256(soff + (shards ? sizeof(int32_t) * std::min<long long>(n, kMaxPieces) : 0));
   const size_t o_psh = soff; soff = align256(soff + (shards ? sizeof(int32_t) * n : 0));
   const size_t sbytes = soff;
@@ -712,7 +801,6 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   int32_t* po = reinterpret_cast<int32_t*>(scratch + o_po);
   long long* partials = reinterpret_cast<long long*>(scratch + o_part);
   long long* totals = reinterpret_cast<long long*>(scratch + o_tot);
-  auto* pkeys = reinterpret_cast<unsigned long long*>(scratch + o_pkey);
   auto* rem = reinterpret_cast<int32_t*>(scratch + o_rem);
   auto* piece_shard = reinterpret_cast<int32_t*>(scratch + o_psh);
 
@@ -724,11 +812,13 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
                                                    tos, po);
   note_launch();
   if (shards) {
-    k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, d_lengths, pkeys);
+    const RadixScratch ps = radix_scratch(scratch + o_pkey, n);
+    k_piece_keys<<<grid_for(n, 256), 256, 0, st>>>(n, capacity, d_lengths, ps.k0);
     note_launch();
-    e = sort_keys(pkeys, n, st);
+    const uint32_t *sorted_keys = nullptr, *sorted_docs = nullptr;
+    e = radix_sort(ps, n, static_cast<uint32_t>(capacity), st, &sorted_keys, &sorted_docs);
     if (e != cudaSuccess) return cleanup(fail_cuda(e, "piece sort"));
-    k_shard_bfd<<<1, kBfdThreads, 0, st>>>(pkeys, capacity, totals, rem, piece_shard);
+    k_shard_bfd<<<1, kBfdThreads, 0, st>>>(sorted_keys, sorted_docs, capacity, totals, rem, piece_shard);
     note_launch();
   }
   e = cudaGetLastError();
@@ -772,18 +862,16 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
   int32_t* tiles_f = reinterpret_cast<int32_t*>(m2 + o_tf);
   int32_t* tiles_s = split_list ? reinterpret_cast<int32_t*>(m2 + o_ts) : nullptr;
 
-  // sort scratch: keys (power of two) + unsorted rows
-  const long long sort_n = std::max({ntf, split_list ? nts : 0ll, 2ll});
-  const long long n2 = next_pow2(sort_n);
-  const long long nrows = std::max(ntf, split_list ? nts : 0ll);
+  // sort scratch: radix-sort buffers + unsorted rows
+  const long long nrows = std::max({ntf, split_list ? nts : 0ll, 1ll});
   char* sort_mem = nullptr;
-  const size_t o_keys = 0;
-  size_t so = align256(sizeof(unsigned long long) * n2);
+  size_t so = radix_scratch_bytes(nrows);
   const size_t o_rows = so; so = align256(so + sizeof(int32_t) * 8 * nrows);
   e = cudaMallocAsync(reinterpret_cast<void**>(&sort_mem), so, st);
   if (e != cudaSuccess) return cleanup(fail_cuda(e, "cudaMallocAsync(plan sort scratch)"));
-  auto* keys = reinterpret_cast<unsigned long long*>(sort_mem + o_keys);
+  const RadixScratch rs = radix_scratch(sort_mem, nrows);
   auto* rows = reinterpret_cast<int32_t*>(sort_mem + o_rows);
+  const uint32_t *sorted_keys = nullptr, *perm = nullptr;
   auto cleanup2 = [&](hdp_status_t s) {
     cudaFreeAsync(sort_mem, st);
     return cleanup(s);
@@ -799,19 +887,22 @@ extern "C" hdp_status_t hdp_plan_create_ex(const int32_t* d_lengths, int32_t num
     note_launch();
   }
   // fused work list
-  k_fill_tiles_fused<<<grid_for(ntf, 256), 256, 0, st>>>(n, ntf, cu, tof, rows, keys);
+  // heaviest first: weights are 1 .. ceil(longest document / 128)
+  const int32_t w_max = static_cast<int32_t>((h_tot[6] + kTile - 1) / kTile);
+  k_fill_tiles_fused<<<grid_for(ntf, 256), 256, 0, st>>>(n, ntf, cu, tof, w_max, rows, rs.k0);
   note_launch();
-  e = sort_keys(keys, ntf, st);
+  e = radix_sort(rs, ntf, static_cast<uint32_t>(w_max - 1), st, &sorted_keys, &perm);
   if (e != cudaSuccess) return cleanup2(fail_cuda(e, "work list sort"));
-  k_gather_rows<<<grid_for(ntf, 256), 256, 0, st>>>(keys, ntf, rows, tiles_f);
+  k_gather_rows<<<grid_for(ntf, 256), 256, 0, st>>>(perm, ntf, rows, tiles_f);
   note_launch();
   // split work list
   if (split_list && nts > 0) {
-    k_fill_tiles_split<<<grid_for(nts, 256), 256, 0, st>>>(n, capacity, nts, cu, bo, tos, rows, keys);
+    // weights are 1 .. C / 128
+    k_fill_tiles_split<<<grid_for(nts, 256), 256, 0, st>>>(n, capacity, nts, cu, bo, tos, rows, rs.k0);
     note_launch();
-    e = sort_keys(keys, nts, st);
+    e = radix_sort(rs, nts, static_cast<uint32_t>(capacity / kTile - 1), st, &sorted_keys, &perm);
     if (e != cudaSuccess) return cleanup2(fail_cuda(e, "split work list sort"));
-    k_gather_rows<<<grid_for(nts, 256), 256, 0, st>>>(keys, nts, rows, tiles_s);
+    k_gather_rows<<<grid_for(nts, 256), 256, 0, st>>>(perm, nts, rows, tiles_s);
     note_launch();
   }
   e = cudaGetLastError();
