@@ -539,6 +539,41 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const uint32_t*
   }
 }
 
+// Small inputs (n <= kSmallSort) in one launch: one CTA sorts (key, index)
+// pairs packed as key << 32 | index with a bitonic network in shared memory
+// (the index makes the order that of a stable sort by key).
+constexpr int kSmallSort = 4096;
+constexpr int kSmallSortThreads = 1024;
+__global__ void __launch_bounds__(kSmallSortThreads) k_sort_small(const uint32_t* __restrict__ keys, int n,
+                                                                  uint32_t* __restrict__ keys_out,
+                                                                  uint32_t* __restrict__ perm_out) {
+  __shared__ unsigned long long s[kSmallSort];
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += kSmallSortThreads)
+    s[i] = i < n ? (static_cast<unsigned long long>(keys[i]) << 32) | static_cast<unsigned>(i) : ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2 / 2; i += kSmallSortThreads) {
+        const int lo = (i / j) * 2 * j + (i % j);
+        const int hi = lo + j;
+        const bool asc = (lo & k) == 0;
+        const unsigned long long a = s[lo], b = s[hi];
+        if ((a > b) == asc) {
+          s[lo] = b;
+          s[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += kSmallSortThreads) {
+    keys_out[i] = static_cast<uint32_t>(s[i] >> 32);
+    perm_out[i] = static_cast<uint32_t>(s[i] & 0xffffffffu);
+  }
+}
+
 // out row i = rows[perm[i]] (perm == nullptr: the identity).
 __global__ void k_gather_rows(const uint32_t* __restrict__ perm, long long count, const int32_t* __restrict__ rows,
                               int32_t* __restrict__ out) {
@@ -702,12 +737,19 @@ RadixScratch radix_scratch(char* mem, long long n) {
 }
 
 // Stable sort of the n keys in sc.k0 (every key <= max_key) with their
-// indices.  *keys / *perm receive the sorted keys and the source index of
+// indices: one launch when n <= kSmallSort, else the radix passes.  *keys / *perm receive the sorted keys and the source index of
 // each position (perm == nullptr when no pass was needed: the identity,
 // keys == sc.k0).
 cudaError_t radix_sort(RadixScratch sc, long long n, uint32_t max_key, cudaStream_t st, const uint32_t** keys,
                        const uint32_t** perm) {
   const int passes = (bit_length(max_key) + 7) / 8;
+  if (passes > 0 && n > 1 && n <= kSmallSort) {
+    k_sort_small<<<1, kSmallSortThreads, 0, st>>>(sc.k0, static_cast<int>(n), sc.k1, sc.v1);
+    note_launch();
+    *keys = sc.k1;
+    *perm = sc.v1;
+    return cudaGetLastError();
+  }
   const int nb = static_cast<int>((n + kRadixTile - 1) / kRadixTile);
   uint32_t *kin = sc.k0, *vin = nullptr, *kout = sc.k1, *vout = sc.v1;
   for (int p = 0; p < passes && n > 0; ++p) {
