@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const uint32_t*
   for (int j = 0; j < kRadixItems; ++j) {
 #pragma unroll
     for (int e = lane; e < kRadixThreads; e += 32) wcnt[warp][e] = 0;
-    __syncthreads();  // (round 0: also orders base_d)
+    __syncthreads();  // (first j: also orders base_d)
     const long long i = base + j * kRadixThreads + threadIdx.x;
     const bool valid = i < n;
     const uint32_t key = valid ? keys_in[i] : 0u;
