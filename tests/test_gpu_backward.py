@@ -96,6 +96,19 @@ def test_small_cases(lengths, hq, hkv, d, C):
     full_bwd_parity(lengths, hq, hkv, d, C, seed=len(lengths))
 
 
+def test_many_tiny_documents_and_odd_capacity():
+    """200 documents of 1 to 40 tokens (key tiles straddling many document
+    boundaries) with C = 100, which the backward does not depend on."""
+    rng = np.random.default_rng(17)
+    lengths = [int(x) for x in rng.integers(1, 41, 200)]
+    full_bwd_parity(lengths, 4, 1, 64, 100, seed=19)
+
+
+def test_one_kv_head_for_32_query_heads():
+    """Multi-query attention: dK and dV sum over a GQA group of 32."""
+    full_bwd_parity([700, 300, 129], 32, 1, 128, 256, seed=23)
+
+
 def test_large_logits():
     """Q and K with standard deviation 3 (scores of standard deviation 9
     nats): sharply peaked rows of P."""

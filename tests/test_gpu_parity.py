@@ -263,6 +263,13 @@ def test_many_tiny_documents(mode):
     full_parity(lengths, 4, 1, 64, 128, mode, seed=11)
 
 
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_one_kv_head_for_32_query_heads(mode):
+    """Multi-query attention: a GQA group of 32, so 16 slot pairs share every
+    K/V tile."""
+    full_parity([700, 300, 129], 32, 1, 128, 256, mode, seed=13)
+
+
 def test_capacity_not_a_tile_multiple():
     """FUSED does not depend on C; SPLIT's blocks must be whole tiles, so a
     capacity that is not a multiple of 128 is refused for it."""
