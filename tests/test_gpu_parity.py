@@ -264,6 +264,45 @@ def test_many_tiny_documents(mode):
 
 
 @pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_one_token_documents_closed_form(mode):
+    """1,000 one-token documents: each query sees only its own key, P = 1, so O
+    is V exactly (bit for bit after bf16 rounding) and LSE = scale q.k."""
+    n, hq, hkv, d = 1000, 4, 2, 128
+    w = wl.Workload("case", tuple([1] * n), 128, hq, hkv, d, 1.0, 31)
+    q, k, v = wl.qkv(w, device="cuda")
+    o, lse, plan = run_gpu(q, k, v, [1] * n, 128, mode)
+    plan.destroy()
+    grp = hq // hkv
+    v_rep = v.repeat_interleave(grp, dim=1)
+    assert torch.equal(o, v_rep)
+    k_rep = k.repeat_interleave(grp, dim=1).double()
+    ref = (q.double() * k_rep).sum(-1) * w.scale  # [T][hq]
+    assert torch.allclose(lse.double(), ref.t(), atol=2e-3, rtol=0)
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_zero_keys_closed_form(mode):
+    """K = 0: every score is 0, so each query attends uniformly to its causal
+    prefix: O_p = mean(v_0 .. v_p) of its document, LSE_p = ln(p + 1)."""
+    lengths, hq, hkv, d, C = [300, 1, 650], 4, 2, 64, 256
+    w = wl.Workload("case", tuple(lengths), C, hq, hkv, d, 1.0, 37)
+    q, k, v = wl.qkv(w, device="cuda")
+    k = torch.zeros_like(k)
+    o, lse, plan = run_gpu(q, k, v, lengths, C, mode)
+    plan.destroy()
+    grp = hq // hkv
+    vd = v.double().repeat_interleave(grp, dim=1)
+    start = 0
+    for s in lengths:
+        seg = vd[start:start + s]
+        cnt = torch.arange(1, s + 1, dtype=torch.float64, device="cuda")
+        mean = seg.cumsum(0) / cnt[:, None, None]
+        assert (o[start:start + s].double() - mean).abs().max().item() <= 1.5e-2
+        assert (lse[:, start:start + s].double() - torch.log(cnt)[None, :]).abs().max().item() <= 2e-3
+        start += s
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
 def test_one_kv_head_for_32_query_heads(mode):
     """Multi-query attention: a GQA group of 32, so 16 slot pairs share every
     K/V tile."""
