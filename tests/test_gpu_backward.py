@@ -96,6 +96,20 @@ def test_small_cases(lengths, hq, hkv, d, C):
     full_bwd_parity(lengths, hq, hkv, d, C, seed=len(lengths))
 
 
+def test_one_token_documents_closed_form():
+    """One-token documents: P = 1, so dV is the sum of dO over the GQA group's
+    query heads, and dS = P (dP - D) = 0 with dP = D = dO . v: dQ = dK = 0 up to
+    the rounding of dP (tensor core) against D (row sum)."""
+    n, hq, hkv, d = 1000, 4, 2, 128
+    q, k, v, do = _inputs([1] * n, hq, hkv, d, 41)
+    dq, dk, dv = run_bwd(q, k, v, do, [1] * n, 128)
+    grp = hq // hkv
+    ref_dv = do.double().view(n, hkv, grp, d).sum(2).numpy()
+    compare("dv", dv, ref_dv)
+    assert np.abs(dq).max() <= 1e-2 * float(np.abs(q.float().numpy()).max())
+    assert np.abs(dk).max() <= 1e-2 * float(np.abs(k.float().numpy()).max())
+
+
 def test_many_tiny_documents_and_odd_capacity():
     """200 documents of 1 to 40 tokens (key tiles straddling many document
     boundaries) with C = 100, which the backward does not depend on."""
