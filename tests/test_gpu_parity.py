@@ -378,6 +378,16 @@ def test_seq2m_sampled_chunks():
     sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq2m chunks {chunks}")
 
 
+def test_plan_radix_passes_on_mixed_lengths():
+    """A work list that needs the multi-block, two-pass radix sort: 50 documents
+    of 100K to 200K tokens among 10,000 short ones (about 80,000 fused query
+    tiles with weights up to ~1,600; 10,050 best-fit keys of 14 bits)."""
+    rng = np.random.default_rng(29)
+    lengths = [int(x) for x in rng.integers(100_000, 200_001, 50)] + [int(x) for x in rng.integers(1, 501, 10_000)]
+    rng.shuffle(lengths)
+    check_plan(lengths, 8192)
+
+
 def test_plan_stress_many_documents():
     """2^24 random lengths (plan scan over 8,192 CTAs of documents), without shards."""
     rng = np.random.default_rng(24)
