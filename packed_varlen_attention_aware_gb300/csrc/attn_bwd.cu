@@ -117,6 +117,7 @@ struct BwdParams {
   __nv_bfloat16* dk;     // [T][hkv][D]
   __nv_bfloat16* dv;
   unsigned int* err;
+  long long wait_budget;  // clocks before a role's wait gives up (drain waits keep their own budget)
 };
 
 struct BwdUnit {
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const long long u = bwd_unit_index(k, cta, nctas);
         if (u >= total_units) break;
         const BwdUnit x = bwd_unit(p, u);
-        if (units > 0 && !mbar_wait(&bars.kv_empty, (units - 1) & 1, abort_word, p.err, kErrBKvE)) {
+        if (units > 0 && !mbar_wait(&bars.kv_empty, (units - 1) & 1, abort_word, p.err, kErrBKvE, p.wait_budget)) {
           ok = false;
           break;
         }
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int h = x.kvh * p.group, i = x.n - 1;  // query head and tile of iteration it
         for (int it = 0; it < x.iters; ++it) {
           const int q_row0 = x.doc_start + i * kTile;
-          if (qround > 0 && !mbar_wait(&bars.q_empty[qs], (qround - 1) & 1, abort_word, p.err, kErrBQE)) {
+          if (qround > 0 && !mbar_wait(&bars.q_empty[qs], (qround - 1) & 1, abort_word, p.err, kErrBQE, p.wait_budget)) {
             q_armed = g;
             ok = false;
             break;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d(smem + L::kQ + qs * L::kTileBytes + hb * L::kHalfBytes, &tmQ, &bars.q_full[qs], hb * 64, h,
                         q_row0);
           const int ds = static_cast<int>(g & 1);
-          if (g >= 2 && !mbar_wait(&bars.do_empty[ds], ((g >> 1) - 1) & 1, abort_word, p.err, kErrBQE)) {
+          if (g >= 2 && !mbar_wait(&bars.do_empty[ds], ((g >> 1) - 1) & 1, abort_word, p.err, kErrBQE, p.wait_budget)) {
             q_armed = g + 1;
             ok = false;
             break;
@@ -349,10 +350,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int it = 0;
       if (ok) {
         x = bwd_unit(p, u);
-        ok = mbar_wait(&bars.kv_full, 0, abort_word, p.err, kErrBKv) &&
-             mbar_wait(&bars.q_full[0], 0, abort_word, p.err, kErrBQ);
+        ok = mbar_wait(&bars.kv_full, 0, abort_word, p.err, kErrBKv, p.wait_budget) &&
+             mbar_wait(&bars.q_full[0], 0, abort_word, p.err, kErrBQ, p.wait_budget);
         if (ok) issue_s(0);
-        if (ok) ok = mbar_wait(&bars.do_full[0], 0, abort_word, p.err, kErrBQ);
+        if (ok) ok = mbar_wait(&bars.do_full[0], 0, abort_word, p.err, kErrBQ, p.wait_budget);
         if (ok) {
           issue_dp(0);
           if (x.iters == 1) umma_commit(&bars.kv_empty);
@@ -362,9 +363,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool first = it == 0, last = it == x.iters - 1;
         const int ds = static_cast<int>(g & 1);
         // dV += P^T dO_g, once the compute warps have written P(g)
-        ok = mbar_wait(&bars.p_full, g & 1, abort_word, p.err, kErrBP);
+        ok = mbar_wait(&bars.p_full, g & 1, abort_word, p.err, kErrBP, p.wait_budget);
         if (ok && first && units > 0)
-          ok = mbar_wait(&bars.dkv_empty, (units - 1) & 1, abort_word, p.err, kErrBDkvE);
+          ok = mbar_wait(&bars.dkv_empty, (units - 1) & 1, abort_word, p.err, kErrBDkvE, p.wait_budget);
         if (!ok) break;
         tc_fence_after();
         {
@@ -385,13 +386,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (has_next) xn = bwd_unit(p, un);
         }
         if (has_next) {
-          if (next_new_unit) ok = mbar_wait(&bars.kv_full, (units + 1) & 1, abort_word, p.err, kErrBKv);
-          if (ok) ok = mbar_wait(&bars.q_full[qs_next], ((g + 1) / L::kQStages) & 1, abort_word, p.err, kErrBQ);
+          if (next_new_unit) ok = mbar_wait(&bars.kv_full, (units + 1) & 1, abort_word, p.err, kErrBKv, p.wait_budget);
+          if (ok) ok = mbar_wait(&bars.q_full[qs_next], ((g + 1) / L::kQStages) & 1, abort_word, p.err, kErrBQ, p.wait_budget);
           if (!ok) break;
           issue_s(qs_next);
         }
         // dK += dS^T Q_g, once the compute warps have written dS(g)
-        ok = mbar_wait(&bars.ds_full, g & 1, abort_word, p.err, kErrBP);
+        ok = mbar_wait(&bars.ds_full, g & 1, abort_word, p.err, kErrBP, p.wait_budget);
         if (!ok) break;
         tc_fence_after();
         {
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(&bars.q_empty[qs]);
         if (last) umma_commit(&bars.dkv_full);
         if (!has_next) break;
-        ok = mbar_wait(&bars.do_full[ds ^ 1], ((g + 1) >> 1) & 1, abort_word, p.err, kErrBQ);
+        ok = mbar_wait(&bars.do_full[ds ^ 1], ((g + 1) >> 1) & 1, abort_word, p.err, kErrBQ, p.wait_budget);
         if (!ok) break;
         issue_dp(ds ^ 1);
         // K and V of a unit are read last by the S and dP of its last tile
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       for (int it = 0; it < x.iters; ++it) {
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_word, p.err, kErrBS));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_word, p.err, kErrBS, p.wait_budget));
         const int q_base = i * kTile;
         const int c_lo = key_local - q_base;  // query column c allowed iff c_lo <= c < c_hi
         const int c_hi = x.doc_len - q_base;
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (it + 1 < x.iters) pre = staged(x, nh, ni);
         // ---- dS phase
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, g & 1, abort_word, p.err, kErrBS));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, g & 1, abort_word, p.err, kErrBS, p.wait_budget));
         if (ok) {
           tc_fence_after();
           uint32_t dpv[2][32];
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       // ---- the unit's dK and dV rows (thread = key row)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkv_full, units & 1, abort_word, p.err, kErrBDkv));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkv_full, units & 1, abort_word, p.err, kErrBDkv, p.wait_budget));
       if (named_barrier_or(kDsBarrier, 256, !ok)) {
         ok = false;
         break;
@@ -768,7 +769,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const long long u = bwd_unit_index(k, cta, nctas);
         if (u >= total_units) break;
         const DqUnit x = dq_unit(p, u);
-        if (units > 0 && !mbar_wait(&bars.q_empty, (units - 1) & 1, abort_word, p.err, kErrDQE)) {
+        if (units > 0 && !mbar_wait(&bars.q_empty, (units - 1) & 1, abort_word, p.err, kErrDQE, p.wait_budget)) {
           ok = false;
           break;
         }
@@ -781,7 +782,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++units;
         for (int j = 0; j < x.ntk; ++j) {
           const int row0 = x.doc_start + j * kTile;
-          if (kround > 0 && !mbar_wait(&bars.k_empty[ks], (kround - 1) & 1, abort_word, p.err, kErrDKvE)) {
+          if (kround > 0 && !mbar_wait(&bars.k_empty[ks], (kround - 1) & 1, abort_word, p.err, kErrDKvE, p.wait_budget)) {
             k_armed = kvc;
             ok = false;
             break;
@@ -792,7 +793,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d(smem + L::kK + ks * L::kTileBytes + hb * L::kHalfBytes, &tmK, &bars.k_full[ks], hb * 64,
                         x.kvh, row0);
           const int vs = static_cast<int>(kvc & 1);
-          if (kvc >= 2 && !mbar_wait(&bars.v_empty[vs], ((kvc >> 1) - 1) & 1, abort_word, p.err, kErrDKvE)) {
+          if (kvc >= 2 && !mbar_wait(&bars.v_empty[vs], ((kvc >> 1) - 1) & 1, abort_word, p.err, kErrDKvE, p.wait_budget)) {
             k_armed = kvc + 1;
             ok = false;
             break;
@@ -842,9 +843,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       // dQ += dS(t) K(t) for global tile t (its dS sits in S buffer t & 1, its K in stage kst)
       auto issue_dq = [&](long long t, int kst, bool first_of_unit) -> bool {
-        if (!mbar_wait(&bars.p_full[t & 1], (t >> 1) & 1, abort_word, p.err, kErrDP)) return false;
+        if (!mbar_wait(&bars.p_full[t & 1], (t >> 1) & 1, abort_word, p.err, kErrDP, p.wait_budget)) return false;
         if (first_of_unit && units > 0 &&
-            !mbar_wait(&bars.dq_empty, (units - 1) & 1, abort_word, p.err, kErrDDqE))
+            !mbar_wait(&bars.dq_empty, (units - 1) & 1, abort_word, p.err, kErrDDqE, p.wait_budget))
           return false;
         tc_fence_after();
         const uint32_t a = tS0 + static_cast<uint32_t>(t & 1) * 128u;
@@ -860,11 +861,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const long long u = bwd_unit_index(k, cta, nctas);
         if (u >= total_units) break;
         const DqUnit x = dq_unit(p, u);
-        ok = mbar_wait(&bars.q_full, units & 1, abort_word, p.err, kErrDQ);
+        ok = mbar_wait(&bars.q_full, units & 1, abort_word, p.err, kErrDQ, p.wait_budget);
         if (!ok) break;
         for (int j = 0; j < x.ntk && ok; ++j) {
           const int st = static_cast<int>(kvc & 1);
-          ok = mbar_wait(&bars.k_full[ks], kround & 1, abort_word, p.err, kErrDKv);
+          ok = mbar_wait(&bars.k_full[ks], kround & 1, abort_word, p.err, kErrDKv, p.wait_budget);
           if (!ok) break;
           // S(j) into buffer st: its previous dS was read by a dQ MMA issued earlier
           const uint64_t kd = dK_k + static_cast<uint64_t>(ks) * kTileUnits;
@@ -875,11 +876,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           // dP(j) once the compute warps have read dP(j-1)
           if (kvc > 0) {
-            ok = mbar_wait(&bars.dp_free, (kvc - 1) & 1, abort_word, p.err, kErrDDp);
+            ok = mbar_wait(&bars.dp_free, (kvc - 1) & 1, abort_word, p.err, kErrDDp, p.wait_budget);
             if (!ok) break;
             tc_fence_after();
           }
-          ok = mbar_wait(&bars.v_full[st], (kvc >> 1) & 1, abort_word, p.err, kErrDKv);
+          ok = mbar_wait(&bars.v_full[st], (kvc >> 1) & 1, abort_word, p.err, kErrDKv, p.wait_budget);
           if (!ok) break;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -934,7 +935,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2), s2 = pack_f32x2(p.scale, p.scale);
       const uint64_t nl2 = pack_f32x2(-lse2, -lse2), nd2 = pack_f32x2(-dlr * p.scale, -dlr * p.scale);
       for (int j = 0; j < x.ntk; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, tg & 1, abort_word, p.err, kErrDS));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, tg & 1, abort_word, p.err, kErrDS, p.wait_budget));
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tS0 + static_cast<uint32_t>(tg & 1) * 128u;
@@ -987,7 +988,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- dQ of the unit -> bf16 rows
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, units & 1, abort_word, p.err, kErrDDq));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, units & 1, abort_word, p.err, kErrDDq, p.wait_budget));
       if (!ok) break;
       tc_fence_after();
       __nv_bfloat16* out = p.dq + (tok * p.hq + x.h) * static_cast<long long>(D) + hf * (D / 2);
@@ -1097,6 +1098,7 @@ hdp_status_t launch_bwd(const hdp_plan_s* plan, const void* q, const void* k, co
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.err = device_error_word();
   if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
+  prm.wait_budget = wait_budget_clocks();
   // dK, dV: one unit per (key tile, kv head)
   {
     const long long units = prm.ntiles * hkv;

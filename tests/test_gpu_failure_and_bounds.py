@@ -71,6 +71,43 @@ def test_expired_wait_reports_timeout_and_the_next_call_recovers():
     full_parity([300, 1, 255, 513], 8, 2, 128, 256, SPLIT)
 
 
+def test_backward_expired_wait_reports_timeout_and_the_next_call_recovers():
+    """The backward's two kernels take the same wait budget: with one clock the
+    first unsatisfied wait expires, every role stops and drains, the status
+    reads HDP_ERR_DEVICE_TIMEOUT, and the next call is correct."""
+    lengths, hq, hkv, d, C = [64], 2, 1, 64, 128
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(64, hq, d, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(64, hkv, d, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(64, hkv, d, generator=g).to(torch.bfloat16).cuda()
+    do = torch.randn(64, hq, d, generator=g).to(torch.bfloat16).cuda()
+    dl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    pkg.hdp_device_status()
+    o, lse, plan = pkg.attention(q, k, v, dl, C)
+    try:
+        pkg.hdp_set_wait_budget(1)
+        try:
+            pkg.attention_backward(plan, q, k, v, o, lse, do)
+            torch.cuda.synchronize()  # both kernels returned
+        finally:
+            pkg.hdp_set_wait_budget(0)
+        with pytest.raises(pkg.HdpError) as e:
+            pkg.hdp_device_status()
+        assert e.value.status == pkg.HDP_ERR_DEVICE_TIMEOUT
+        pkg.hdp_device_status()
+        dq, dk, dv = pkg.attention_backward(plan, q, k, v, o, lse, do)
+        pkg.hdp_device_status()
+    finally:
+        plan.destroy()
+    bits = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    cu = np.array([0, 64], np.int32)
+    refs = oracle.attention_bwd(bits(q), bits(k), bits(v), bits(do), cu, hq, hkv, d, 1.0 / d ** 0.5)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        err = np.abs(got.float().cpu().numpy() - ref)
+        assert err.max() <= 2e-2 * np.abs(ref).max() + 1e-6, name
+
+
 # ---------------------------------------------------------------- guard bands
 
 def _guarded(nbytes):
