@@ -262,8 +262,9 @@ uint64_t hdp_kernel_launch_count(void);
 uint64_t hdp_host_sync_count(void);
 
 /*
- * Budget of the attention forward's bounded waits, in SM clocks, for the
- * launches this process makes after the call (all devices, all threads).
+ * Budget of the bounded waits of the attention forward and backward kernels,
+ * in SM clocks, for the launches this process makes after the call (all
+ * devices, all threads).
  * clocks <= 0 restores the default of 2e9 clocks (about one second at
  * 2 GHz); no legitimate wait lasts more than a few microseconds.  A budget of
  * a few clocks makes the first wait that is not already satisfied expire: the
