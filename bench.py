@@ -472,94 +472,110 @@ def our_arm(args, ws, rank, local):
     e2e_steps = min(args.steps, 3) if long_step else args.steps
     e2e_warm = 1 if long_step else max(2, args.warmup // 2)
 
-    def pinned_like(t):
-        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    def run_e2e():
+        """The end-to-end leg; returns ((e2e_ms, h2d, d2h, rates), None), or
+        (None, reason) when the pinned host buffers cannot be had on every rank."""
+        def pinned_like(t):
+            return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
 
-    qh, kh, vh = pinned_like(q), pinned_like(k), pinned_like(v)
-    qh.copy_(q)
-    kh.copy_(k)
-    vh.copy_(v)
-    lh = torch.tensor(w.lengths, dtype=torch.int32).pin_memory()
-    oh, lseh, fh = pinned_like(o), pinned_like(lse), pinned_like(shard_flops)
-    qd = [q, torch.empty_like(q)]
-    kd = [k, torch.empty_like(k)]
-    vd = [v, torch.empty_like(v)]
-    ld = [torch.empty_like(lengths_d), torch.empty_like(lengths_d)]
-    od = [o, torch.empty_like(o)]
-    lsed = [lse, torch.empty_like(lse)]
-    fd = [shard_flops, torch.empty_like(shard_flops)]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_done = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
-    def upload(i):
-        b = i & 1
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_out[b])  # the slot's previous outputs are home, its inputs no longer read
-            qd[b].copy_(qh, non_blocking=True)
-            kd[b].copy_(kh, non_blocking=True)
-            vd[b].copy_(vh, non_blocking=True)
-            ld[b].copy_(lh, non_blocking=True)
-            ev_in[b].record(s_in)
+        err = None
+        try:
+            qh, kh, vh = pinned_like(q), pinned_like(k), pinned_like(v)
+            qh.copy_(q)
+            kh.copy_(k)
+            vh.copy_(v)
+            lh = torch.tensor(w.lengths, dtype=torch.int32).pin_memory()
+            oh, lseh, fh = pinned_like(o), pinned_like(lse), pinned_like(shard_flops)
+        except RuntimeError as exc:
+            err = "pinned host buffers: " + str(exc).splitlines()[0][:160]
+        flag = torch.tensor([0 if err else 1], dtype=torch.int32, device=dev)
+        if ws > 1:
+            dist.all_reduce(flag, op=dist.ReduceOp.MIN)
+        if int(flag.item()) == 0:
+            return None, err or "another rank could not pin its host buffers"
+        qd = [q, torch.empty_like(q)]
+        kd = [k, torch.empty_like(k)]
+        vd = [v, torch.empty_like(v)]
+        ld = [torch.empty_like(lengths_d), torch.empty_like(lengths_d)]
+        od = [o, torch.empty_like(o)]
+        lsed = [lse, torch.empty_like(lse)]
+        fd = [shard_flops, torch.empty_like(shard_flops)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        def upload(i):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_out[b])  # the slot's previous outputs are home, its inputs no longer read
+                qd[b].copy_(qh, non_blocking=True)
+                kd[b].copy_(kh, non_blocking=True)
+                vd[b].copy_(vh, non_blocking=True)
+                ld[b].copy_(lh, non_blocking=True)
+                ev_in[b].record(s_in)
 
-    def compute_and_download(i):
-        b = i & 1
-        stream.wait_event(ev_in[b])
-        plan = pkg.hdp_plan_create(ld[b], w.capacity, flags=plan_flags, stream=stream)
-        pkg.hdp_attention_fwd(plan, qd[b], kd[b], vd[b], w.hq, w.hkv, w.d, w.scale, mode, workspace, od[b], lsed[b],
-                              stream=stream)
-        pkg.hdp_flops_per_shard(plan, w.d, w.hq, fd[b], stream=stream)
-        ev_done[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[b])
-            oh.copy_(od[b], non_blocking=True)
-            lseh.copy_(lsed[b], non_blocking=True)
-            fh.copy_(fd[b], non_blocking=True)
+        def compute_and_download(i):
+            b = i & 1
+            stream.wait_event(ev_in[b])
+            plan = pkg.hdp_plan_create(ld[b], w.capacity, flags=plan_flags, stream=stream)
+            pkg.hdp_attention_fwd(plan, qd[b], kd[b], vd[b], w.hq, w.hkv, w.d, w.scale, mode, workspace, od[b], lsed[b],
+                                  stream=stream)
+            pkg.hdp_flops_per_shard(plan, w.d, w.hq, fd[b], stream=stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                oh.copy_(od[b], non_blocking=True)
+                lseh.copy_(lsed[b], non_blocking=True)
+                fh.copy_(fd[b], non_blocking=True)
+                ev_out[b].record(s_out)
+            plan.destroy()
+
+        def e2e_run(steps):
+            upload(0)
+            for i in range(steps):
+                if i + 1 < steps:
+                    upload(i + 1)
+                compute_and_download(i)
+
+        for b in range(2):
             ev_out[b].record(s_out)
-        plan.destroy()
-
-    def e2e_run(steps):
-        upload(0)
-        for i in range(steps):
-            if i + 1 < steps:
-                upload(i + 1)
-            compute_and_download(i)
-
-    for b in range(2):
-        ev_out[b].record(s_out)
-    e2e_run(e2e_warm)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_stream(stream)
-    e2e_run(e2e_steps)
-    stream.wait_stream(s_out)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    pkg.hdp_device_status()
-    h2d = in_bytes + lh.numel() * 4
-    d2h = oh.numel() * 2 + lseh.numel() * 4 + fh.numel() * 8
-    # the host link alone, per direction: one step's uploads, then its downloads
-    rates = {}
-    for direction in ("h2d", "d2h"):
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(s_in)
-        with torch.cuda.stream(s_in):
-            if direction == "h2d":
-                qd[1].copy_(qh, non_blocking=True)
-                kd[1].copy_(kh, non_blocking=True)
-                vd[1].copy_(vh, non_blocking=True)
-            else:
-                oh.copy_(od[1], non_blocking=True)
-                lseh.copy_(lsed[1], non_blocking=True)
-        c1.record(s_in)
+        e2e_run(e2e_warm)
         torch.cuda.synchronize()
-        nbytes = in_bytes if direction == "h2d" else oh.numel() * 2 + lseh.numel() * 4
-        rates[direction] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
-    del qh, kh, vh, oh, lseh, qd, kd, vd, od, lsed
+        if ws > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s_in.wait_stream(stream)
+        e2e_run(e2e_steps)
+        stream.wait_stream(s_out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        pkg.hdp_device_status()
+        h2d = in_bytes + lh.numel() * 4
+        d2h = oh.numel() * 2 + lseh.numel() * 4 + fh.numel() * 8
+        # the host link alone, per direction: one step's uploads, then its downloads
+        rates = {}
+        for direction in ("h2d", "d2h"):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(s_in)
+            with torch.cuda.stream(s_in):
+                if direction == "h2d":
+                    qd[1].copy_(qh, non_blocking=True)
+                    kd[1].copy_(kh, non_blocking=True)
+                    vd[1].copy_(vh, non_blocking=True)
+                else:
+                    oh.copy_(od[1], non_blocking=True)
+                    lseh.copy_(lsed[1], non_blocking=True)
+            c1.record(s_in)
+            torch.cuda.synchronize()
+            nbytes = in_bytes if direction == "h2d" else oh.numel() * 2 + lseh.numel() * 4
+            rates[direction] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        del qh, kh, vh, oh, lseh, qd, kd, vd, od, lsed
+        return (e2e_ms, h2d, d2h, rates), None
+
+    e2e_result, e2e_error = run_e2e()
+    e2e_ms, h2d, d2h, rates = e2e_result if e2e_result else (0.0, 0, 0, {})
 
     (ms, e2e_ms, attn_ms_max), job_flops = aggregate_over_ranks([ms, e2e_ms, attn_ms], flops_step, ws, dev)
 
@@ -606,11 +622,13 @@ def our_arm(args, ws, rank, local):
                          "no ncu capture of this kernel on this workload fits the capture size rule; "
                          "see the seq128k entries"},
             "cpu_baseline": cpu,
-            "e2e": {"value": job_throughput(job_flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
-                    "steps": e2e_steps, "warmup": e2e_warm,
-                    "pipeline": "step i+1 upload and step i-1 download overlap step i compute",
-                    "copy_gbs": rates, "numa_node": numa_node, "numa_cpus_bound": numa_cpus},
+            "e2e": ({"value": job_throughput(job_flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
+                     "steps": e2e_steps, "warmup": e2e_warm,
+                     "pipeline": "step i+1 upload and step i-1 download overlap step i compute",
+                     "copy_gbs": rates, "numa_node": numa_node, "numa_cpus_bound": numa_cpus}
+                    if e2e_error is None else
+                    {"value": None, "unit": "TFLOP/s", "error": e2e_error, "numa_node": numa_node}),
             "gpu_launches": launches,
             "clocks": clk,
         }
