@@ -89,8 +89,8 @@ def attn_kernel_source_sha256() -> str:
 # to the value it was captured with.
 PROFILED_TRAFFIC = {
     ("seq128k", "fused"): {
-        "kernel_source_sha256": "dc4361eb5457a15b1bfd3ab3091858467af1f92f46260eb1b20f29d1783cfad5",
-        "dram_bytes_per_launch": 13480086528 + 1090898688,
+        "kernel_source_sha256": "8c23a8430c8ada1741ac12010700bd2dacf6459bc08a3fe02fb6790ec27874d7",
+        "dram_bytes_per_launch": 5338317312 + 1069282304,
         "source": "ncu capture summarised in profiles/attn_fwd_seq128k.md",
     },
 }

@@ -154,6 +154,12 @@ hdp_status_t hdp_attention_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t 
  *   FUSED: o and lse are final.  SPLIT: needs capacity % 128 == 0 and a
  *   workspace of hdp_attention_workspace_bytes; writes the partials there,
  *   then merges them into o and lse with hdp_lse_merge on the same stream.
+ *   Each partial covers exactly its block's C keys.  The kernel either walks
+ *   the SPLIT work list (a unit per block query tile) or walks the fused
+ *   list and writes a partial at every chunk end of a query tile's key
+ *   range; it takes the second unless one kv head's K and V rows of the
+ *   longest document exceed 1.25x the device's L2.  Both give the same
+ *   partials, bit for bit.
  *   q, k, v, o must be 16-byte aligned.
  * Device-side wait timeouts are reported by hdp_device_status.
  */

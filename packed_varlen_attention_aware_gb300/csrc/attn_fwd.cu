@@ -23,7 +23,16 @@
 // The online softmax keeps a stale running max unless it grows by more than
 // 2^8, so O is rescaled only rarely; the final O/l and LSE use the same max, so
 // the result is exact.  In SPLIT mode each block (q chunk, kv chunk) ends in a
-// partial (O fp32, LSE) instead.
+// partial (O fp32, LSE) instead, in one of two ways:
+//   block list  a unit is one query tile of one block (the plan's SPLIT work
+//               list): the unit's key range is that block's C keys
+//   streaming   a unit is FUSED's (a query tile over its whole causal key
+//               range); at each chunk boundary of that range the block just
+//               finished is written and the running max, l and O restart, so
+//               each partial still covers exactly its own C keys, without a
+//               unit restart (a new Q tile, a refilled pipeline) per block
+// The launch picks streaming unless one head's K and V rows of the longest
+// document are much larger than L2 (see launch()).
 //
 // Every mbarrier wait is bounded; a timeout sets the device error word, all
 // roles stop, in-flight copies and MMAs are drained, TMEM is freed.
@@ -56,6 +65,9 @@ constexpr int kSoftmaxRegs = 176;
 constexpr int kControlRegs = 152;
 constexpr int kStages = 2;  // K and V ring depth
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// kernel modes (a template argument, so each mode's code carries no other
+// mode's state or branches: the FUSED softmax warps stay free of spills)
+constexpr int kFused = 0, kSplitList = 1, kSplitStream = 2;
 
 // error codes recorded in the device error word
 constexpr int kErrQFull = 0x101, kErrKFull = 0x102, kErrVFull = 0x103, kErrSFull = 0x104, kErrPFull = 0x105,
@@ -96,7 +108,10 @@ struct Params {
   float* o_part;         // SPLIT partials [N_b][C][hq][D]
   float* lse_part;       // SPLIT partials [N_b][hq][C]
   int C;
-  int split;
+  int tpc;               // streaming SPLIT: key tiles per chunk, C / 128
+  int ndocs;
+  const int32_t* cu;     // streaming SPLIT: cu_seqlens [ndocs + 1]
+  const int64_t* bo;     // streaming SPLIT: first causal block of each document [ndocs + 1]
   unsigned int* err;
   long long wait_budget;  // clocks before a role's wait gives up (drain waits keep their own budget)
 };
@@ -160,10 +175,27 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D>
+// Document holding token `start`: the d < n with cu[d] <= start < cu[d + 1].
+// A 32-way search by the whole warp: each step the lanes probe 32 evenly
+// spaced offsets of [lo, hi) and keep the span after the last one that is
+// <= start, so n documents take ceil(log32 n) steps.
+__device__ __forceinline__ int doc_at(const int32_t* __restrict__ cu, int n, int start, int lane) {
+  int lo = 0, hi = n;  // cu[lo] <= start < cu[hi]
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int idx = lo + lane * step;
+    const unsigned le = __ballot_sync(0xffffffffu, idx < hi && __ldg(cu + idx) <= start);
+    lo += (31 - __clz(le)) * step;  // lane 0 probes lo itself, so le != 0
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
+  constexpr bool kSplit = MODE != kFused, kStream = MODE == kSplitStream;
   using L = SmemLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -342,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 1; kk < kTile / 16; ++kk)
           umma_ts_c<true>(tO(s), tS(s) + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_pv);
       };
-      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};
+      uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0}, units_done[2] = {0, 0};  // units_done: epilogues
       long long g = 0;
       bool ok = true;  // every wait so far succeeded
       auto wait_on = [&](uint64_t* bar, uint32_t parity, int code) {
@@ -361,18 +393,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // branches cost it tens of cycles a MMA.
       // key tile j of the unit; kind 0: steady (j < n - 2), 1: j = n - 2 (Q is
       // free after its S), 2: j = n - 1 (the unit's last P.V)
-      auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind) -> bool {
+      // first / last: key tile j opens / closes an epilogue's span (the unit,
+      // or one C-key chunk in streaming SPLIT); call sites pass constants
+      // where they can, so steady tiles carry no span bookkeeping
+      auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind, bool first, bool last) -> bool {
         for (int s = 0; s < nslots; ++s) {
           if (s == 0) wait_group(kErrVFull);
-          if (j == 0 && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
+          if (first && units_done[s] > 0) wait_on(&bars.o_empty[s], (units_done[s] - 1) & 1, kErrOEmpty);
           wait_on(&bars.p_full[s], p_uses[s] & 1, kErrPFull);  // P_s(j) written, O_s rescaled
           ++p_uses[s];
           if (!ok) return false;
           tc_fence_after();
-          issue_pv(s, vs, j > 0);
-          if (kind == 2) {
+          issue_pv(s, vs, !first);
+          if (last) {
             umma_commit(&bars.o_full[s]);
-          } else {
+            ++units_done[s];
+          }
+          if (kind != 2) {
             issue_qk(s, ks);
             if (kind == 1) umma_commit(&bars.q_empty[s]);
           }
@@ -401,22 +438,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&bars.k_empty[c]);
         int j = 0;
-        if (c == 0) {
-          for (; j + 1 < n - 2 && alive; j += 2)
-            alive = tile(x, nslots, j, 0, 1, 0) && tile(x, nslots, j + 1, 1, 0, 0);
+        if constexpr (kStream) {
+          // span by span: the span's first tile, its steady middle (as in
+          // FUSED: constant stages, no bookkeeping), then its last tile and
+          // the unit's last two (kinds 1 and 2) with flags taken at run time
+          auto kind_of = [n](int jj) { return jj == n - 1 ? 2 : (jj == n - 2 ? 1 : 0); };
+          while (alive && j < n) {
+            const int je = min(j + p.tpc, n);
+            alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), kind_of(j), true, j == je - 1);
+            ++j;
+            const int steady_end = min(je - 1, n - 2);
+            if ((c ^ (j & 1)) == 0) {
+              for (; j + 1 < steady_end && alive; j += 2)
+                alive = tile(x, nslots, j, 0, 1, 0, false, false) && tile(x, nslots, j + 1, 1, 0, 0, false, false);
+            } else {
+              for (; j + 1 < steady_end && alive; j += 2)
+                alive = tile(x, nslots, j, 1, 0, 0, false, false) && tile(x, nslots, j + 1, 0, 1, 0, false, false);
+            }
+            for (; j < steady_end && alive; ++j)
+              alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0, false, false);
+            for (; j < je && alive; ++j)
+              alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), kind_of(j), false, j == je - 1);
+          }
         } else {
-          for (; j + 1 < n - 2 && alive; j += 2)
-            alive = tile(x, nslots, j, 1, 0, 0) && tile(x, nslots, j + 1, 0, 1, 0);
+          if (c == 0) {
+            for (; j + 1 < n - 2 && alive; j += 2)
+              alive = tile(x, nslots, j, 0, 1, 0, j == 0, false) && tile(x, nslots, j + 1, 1, 0, 0, false, false);
+          } else {
+            for (; j + 1 < n - 2 && alive; j += 2)
+              alive = tile(x, nslots, j, 1, 0, 0, j == 0, false) && tile(x, nslots, j + 1, 0, 1, 0, false, false);
+          }
+          for (; j < n - 2 && alive; ++j) alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0, j == 0, false);
+          if (alive && n >= 2) {
+            alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 1, j == 0, false);
+            ++j;
+          }
+          if (alive) alive = tile(x, nslots, j, c ^ (j & 1), 0, 2, j == 0, true);
         }
-        for (; j < n - 2 && alive; ++j) alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 0);
-        if (alive && n >= 2) {
-          alive = tile(x, nslots, j, c ^ (j & 1), c ^ 1 ^ (j & 1), 1);
-          ++j;
-        }
-        if (alive) alive = tile(x, nslots, j, c ^ (j & 1), 0, 2);
         if (!alive) break;
         c ^= n & 1;
-        for (int s = 0; s < nslots; ++s) ++units_done[s];
       }
       // drain every MMA this thread issued before TMEM is released
       umma_commit(&bars.drain);
@@ -448,178 +508,199 @@ __global__ void __launch_bounds__(kThreads, 1)
       // doc-local query position relative to the first key of the range
       const int q_rel = x.q_row0 - x.kv_row0 + row;
       const int key_limit = min(q_rel + 1, x.kv_len);  // keys [0, key_limit) are allowed
-      float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < x.ntiles_kv && ok; ++j) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bars.s_full[s], s_count & 1, abort_word, p.err, kErrSFull, p.wait_budget));
-        if (!ok) break;
-        ++s_count;
-        tc_fence_after();
-        const int lim = key_limit - j * kTile;  // allowed keys of this tile: [0, lim)
-        uint32_t r[4][32];
-        float mc[4];
-        bool rescale_o = false;
-        float alpha = 1.f;
-        // p = 2^(s*scale*log2e - m) for one 32-column chunk: four packed
-        // partial row sums, P packed to bf16 pairs and stored into the first
-        // 64 columns of S (chunk c's keys land in columns [16c, 16c + 16)).
-        auto exp_chunk = [&](int c, uint64_t negm2, uint64_t (&acc)[4]) {
-          uint32_t pk[16];
+      // streaming SPLIT: the tile's chunk qc, its block (qc, 0), its first row
+      // in the chunk
+      int blk0 = 0, row0c = 0;
+      if constexpr (kStream) {
+        const int doc = doc_at(p.cu, p.ndocs, x.kv_row0, lane);
+        const int qc = x.row_off / p.C;
+        blk0 = static_cast<int>(__ldg(p.bo + doc) + static_cast<long long>(qc) * (qc + 1) / 2);
+        row0c = x.row_off - qc * p.C;
+      }
+      // key tiles in spans: the unit's whole range, or one C-key chunk in
+      // streaming SPLIT; each span ends in its own epilogue
+      const int nspan = kStream ? (x.ntiles_kv + p.tpc - 1) / p.tpc : 1;
+      for (int b = 0; b < nspan && ok; ++b) {
+        const int j0 = kStream ? b * p.tpc : 0;
+        const int j1 = kStream ? min(j0 + p.tpc, x.ntiles_kv) : x.ntiles_kv;
+        float m = -INFINITY, l = 0.f;
+        for (int j = j0; j < j1 && ok; ++j) {
+          const bool first = j == j0;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bars.s_full[s], s_count & 1, abort_word, p.err, kErrSFull, p.wait_budget));
+          if (!ok) break;
+          ++s_count;
+          tc_fence_after();
+          const int lim = key_limit - j * kTile;  // allowed keys of this tile: [0, lim)
+          uint32_t r[4][32];
+          float mc[4];
+          bool rescale_o = false;
+          float alpha = 1.f;
+          // p = 2^(s*scale*log2e - m) for one 32-column chunk: four packed
+          // partial row sums, P packed to bf16 pairs and stored into the first
+          // 64 columns of S (chunk c's keys land in columns [16c, 16c + 16)).
+          auto exp_chunk = [&](int c, uint64_t negm2, uint64_t (&acc)[4]) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])),
-                                          scale2, negm2);
-            const float p0 = ex2_approx(lo_f32(t));
-            const float p1 = ex2_approx(hi_f32(t));
-            acc[(i >> 1) & 3] = fadd_f32x2(acc[(i >> 1) & 3], pack_f32x2(p0, p1));
-            pk[i / 2] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS(s) + lane_off + c * 16, pk);
-        };
-        auto row_sum = [](uint64_t (&acc)[4]) {
-          const uint64_t a = fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3]));
-          return lo_f32(a) + hi_f32(a);
-        };
-        if (__all_sync(0xffffffffu, j > 0 && lim >= kTile)) {
-          // Steady tile (no mask, running max known): each chunk's exponentials
-          // are computed with the running max while the next chunk's load is
-          // in flight; a chunk's P only overwrites S columns already loaded.
-          // The row maxima come from the loads themselves.  If one of them
-          // exceeds the running max by more than the threshold, the tile is
-          // recomputed from the registers with the new max (rare).
-          const uint64_t negm2 = pack_f32x2(-m, -m);
-          uint64_t acc[4] = {0, 0, 0, 0};
-          mc[0] = tmem_ld32_max(tS(s) + lane_off, r[0]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (c < 3) mc[c + 1] = tmem_ld32_max(tS(s) + lane_off + (c + 1) * 32, r[c + 1]);
-            exp_chunk(c, negm2, acc);
-            if (c < 3) tmem_wait_ld();
-          }
-          const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
-          const bool grow = mt_scaled > m + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, grow)) {
-            if (grow) {
-              alpha = ex2_approx(m - mt_scaled);
-              l *= alpha;
-              m = mt_scaled;
-              rescale_o = true;
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t t = ffma_f32x2(pack_f32x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])),
+                                            scale2, negm2);
+              const float p0 = ex2_approx(lo_f32(t));
+              const float p1 = ex2_approx(hi_f32(t));
+              acc[(i >> 1) & 3] = fadd_f32x2(acc[(i >> 1) & 3], pack_f32x2(p0, p1));
+              pk[i / 2] = pack_bf16x2(p0, p1);
             }
-            tmem_wait_st();  // the first pass's stores land before they are overwritten
-            const uint64_t negm2n = pack_f32x2(-m, -m);
-            uint64_t acc2[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) exp_chunk(c, negm2n, acc2);
-            l += row_sum(acc2);
-          } else {
-            l += row_sum(acc);
-          }
-        } else {
-          // first tile, or a tile crossing the diagonal or the end of the key
-          // range: load the whole row, mask, take the maximum over the allowed
-          // keys, then the exponentials
-#pragma unroll
-          for (int c = 0; c < 4; ++c) mc[c] = tmem_ld32_max(tS(s) + lane_off + c * 32, r[c]);
-          tmem_wait_ld();
-          if (lim < kTile) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              mc[c] = __uint_as_float(r[c][0]);
-#pragma unroll
-              for (int i = 1; i < 31; i += 2)
-                mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-              mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
-            }
-          }
-          const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
-          if (mt_scaled > m + kRescaleThreshold || j == 0) {
-            const float m_new = fmaxf(m, mt_scaled);
-            alpha = (j == 0) ? 0.f : ex2_approx(m - m_new);
-            l *= alpha;
-            m = m_new;
-            rescale_o = j > 0;
-          }
-          const uint64_t negm2 = pack_f32x2(-m, -m);
-          uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) exp_chunk(c, negm2, acc);
-          l += row_sum(acc);
-        }
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          // P.V of tile j-1 is complete: S_s(j) was committed after it
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO(s) + lane_off + c * 32, o);
+            tmem_st16(tS(s) + lane_off + c * 16, pk);
+          };
+          auto row_sum = [](uint64_t (&acc)[4]) {
+            const uint64_t a = fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3]));
+            return lo_f32(a) + hi_f32(a);
+          };
+          if (__all_sync(0xffffffffu, !first && lim >= kTile)) {
+            // Steady tile (no mask, running max known): each chunk's exponentials
+            // are computed with the running max while the next chunk's load is
+            // in flight; a chunk's P only overwrites S columns already loaded.
+            // The row maxima come from the loads themselves.  If one of them
+            // exceeds the running max by more than the threshold, the tile is
+            // recomputed from the registers with the new max (rare).
+            const uint64_t negm2 = pack_f32x2(-m, -m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            mc[0] = tmem_ld32_max(tS(s) + lane_off, r[0]);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO(s) + lane_off + c * 32, o);
+            for (int c = 0; c < 4; ++c) {
+              if (c < 3) mc[c + 1] = tmem_ld32_max(tS(s) + lane_off + (c + 1) * 32, r[c + 1]);
+              exp_chunk(c, negm2, acc);
+              if (c < 3) tmem_wait_ld();
+            }
+            const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
+            const bool grow = mt_scaled > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, grow)) {
+              if (grow) {
+                alpha = ex2_approx(m - mt_scaled);
+                l *= alpha;
+                m = mt_scaled;
+                rescale_o = true;
+              }
+              tmem_wait_st();  // the first pass's stores land before they are overwritten
+              const uint64_t negm2n = pack_f32x2(-m, -m);
+              uint64_t acc2[4] = {0, 0, 0, 0};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) exp_chunk(c, negm2n, acc2);
+              l += row_sum(acc2);
+            } else {
+              l += row_sum(acc);
+            }
+          } else {
+            // first tile, or a tile crossing the diagonal or the end of the key
+            // range: load the whole row, mask, take the maximum over the allowed
+            // keys, then the exponentials
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mc[c] = tmem_ld32_max(tS(s) + lane_off + c * 32, r[c]);
+            tmem_wait_ld();
+            if (lim < kTile) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (c * 32 + i >= lim) r[c][i] = __float_as_uint(-INFINITY);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                mc[c] = __uint_as_float(r[c][0]);
+#pragma unroll
+                for (int i = 1; i < 31; i += 2)
+                  mc[c] = fmax3(mc[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+                mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+              }
+            }
+            const float mt_scaled = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) * p.scale_log2;
+            if (mt_scaled > m + kRescaleThreshold || first) {
+              const float m_new = fmaxf(m, mt_scaled);
+              alpha = first ? 0.f : ex2_approx(m - m_new);
+              l *= alpha;
+              m = m_new;
+              rescale_o = !first;
+            }
+            const uint64_t negm2 = pack_f32x2(-m, -m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) exp_chunk(c, negm2, acc);
+            l += row_sum(acc);
           }
+          if (__any_sync(0xffffffffu, rescale_o)) {
+            // P.V of tile j-1 is complete: S_s(j) was committed after it
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO(s) + lane_off + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO(s) + lane_off + c * 32, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.p_full[s]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.p_full[s]);
+        if (!ok) break;
+        // ---- epilogue: wait for the span's last P.V, normalize, store
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars.o_full[s], units_done & 1, abort_word, p.err, kErrOFull,
+                                                 p.wait_budget))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool row_valid = row < x.q_rows;
+          const float inv_l = 1.f / l;
+          const float lse_val = (m + __log2f(l)) * 0.69314718055994530942f;
+          const long long tok = static_cast<long long>(x.q_row0) + row;
+          if constexpr (!kSplit) {
+            __nv_bfloat16* dst = p.o + (tok * p.hq + h) * static_cast<long long>(D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO(s) + lane_off + c * 32, o);
+              tmem_wait_ld();
+              if (row_valid) {
+                uint4 w[4];
+                uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  wp[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d4[i] = w[i];
+              }
+            }
+            if (row_valid) p.lse[static_cast<long long>(h) * p.T + tok] = lse_val;
+          } else {
+            const int blk = kStream ? blk0 + b : x.blk;
+            const int r0 = kStream ? row0c : x.row_off;  // the tile's first row in its chunk
+            const long long prow = static_cast<long long>(blk) * p.C + r0 + row;
+            float* dst = p.o_part + (prow * p.hq + h) * static_cast<long long>(D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO(s) + lane_off + c * 32, o);
+              tmem_wait_ld();
+              if (row_valid) {
+                float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                      __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              }
+            }
+            if (row_valid) p.lse_part[(static_cast<long long>(blk) * p.hq + h) * p.C + r0 + row] = lse_val;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.o_empty[s]);
+          ++units_done;
       }
       if (!ok) break;
-      // ---- epilogue: wait for the unit's last P.V, normalize, store
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bars.o_full[s], units_done & 1, abort_word, p.err, kErrOFull, p.wait_budget));
-      if (!ok) break;
-      tc_fence_after();
-      const bool row_valid = row < x.q_rows;
-      const float inv_l = 1.f / l;
-      const float lse_val = (m + __log2f(l)) * 0.69314718055994530942f;
-      const long long tok = static_cast<long long>(x.q_row0) + row;
-      if (!p.split) {
-        __nv_bfloat16* dst = p.o + (tok * p.hq + h) * static_cast<long long>(D);
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO(s) + lane_off + c * 32, o);
-          tmem_wait_ld();
-          if (row_valid) {
-            uint4 w[4];
-            uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              wp[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = w[i];
-          }
-        }
-        if (row_valid) p.lse[static_cast<long long>(h) * p.T + tok] = lse_val;
-      } else {
-        const long long prow = static_cast<long long>(x.blk) * p.C + x.row_off + row;
-        float* dst = p.o_part + (prow * p.hq + h) * static_cast<long long>(D);
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO(s) + lane_off + c * 32, o);
-          tmem_wait_ld();
-          if (row_valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                  __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
-          }
-        }
-        if (row_valid)
-          p.lse_part[(static_cast<long long>(x.blk) * p.hq + h) * p.C + x.row_off + row] = lse_val;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.o_empty[s]);
-      ++units_done;
     }
     tc_fence_before();
     named_barrier_sync(1, kThreads);
@@ -682,9 +763,23 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   if ((r = make_map(&mq, q, T, hq, D)) != HDP_OK) return r;
   if ((r = make_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
+  // SPLIT: streaming unless one head's K and V rows of the longest document
+  // exceed 1.25x L2 (a bound between the two measured cases below).  Streaming units span whole key ranges, and the CTAs of a
+  // round share K/V tiles through L2 only while they stay close together on
+  // the range; the partial writes at chunk ends spread them out, and once the
+  // range no longer fits in L2 the shared tiles are read again from HBM.  The
+  // block list keeps every unit inside one chunk.  (Measured with C = 8,192,
+  // d = 128, one document: streaming was 4 % faster at 128K and 256K tokens,
+  // 134 MB of K and V, and 0.6 % slower at 384K tokens, 201 MB.)
+  int dev = 0, sms = 0, l2 = 0;
+  HDP_CUDA_TRY(cudaGetDevice(&dev));
+  HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  HDP_CUDA_TRY(cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev));
+  const long long kv_head_bytes = 2LL * plan->v.max_doc_len * D * 2;
+  const int mode = !split ? kFused : (4 * kv_head_bytes <= 5LL * l2 ? kSplitStream : kSplitList);
   Params prm{};
-  prm.tiles = split ? plan->v.tiles_split : plan->v.tiles_fused;
-  prm.ntiles = split ? plan->v.num_tiles_split : plan->v.num_tiles_fused;
+  prm.tiles = mode == kSplitList ? plan->v.tiles_split : plan->v.tiles_fused;
+  prm.ntiles = mode == kSplitList ? plan->v.num_tiles_split : plan->v.num_tiles_fused;
   prm.hq = hq;
   prm.hkv = hkv;
   prm.group = hq / hkv;
@@ -696,21 +791,23 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   prm.o_part = o_part;
   prm.lse_part = lse_part;
   prm.C = plan->v.capacity;
-  prm.split = split ? 1 : 0;
+  prm.tpc = plan->v.capacity / kTile;
+  prm.ndocs = plan->v.num_docs;
+  prm.cu = plan->v.cu_seqlens;
+  prm.bo = plan->v.block_offsets;
   prm.err = device_error_word();
   if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
   prm.wait_budget = wait_budget_clocks();
   const long long units = prm.ntiles * hkv * prm.npairs;
   if (units == 0) return HDP_OK;
-  int dev = 0, sms = 0;
-  HDP_CUDA_TRY(cudaGetDevice(&dev));
-  HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int grid = static_cast<int>(units < sms ? units : sms);
   const long long bt = grid / (prm.npairs * heads_per_round(plan->v.max_doc_len, hkv));
   prm.block_tiles = bt > 0 ? bt : 1;
   const int smem = SmemLayout<D>::kBytes + 1024;
-  HDP_CUDA_TRY(cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  k_attn_fwd<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
+  auto kernel = mode == kFused ? k_attn_fwd<D, kFused>
+               : mode == kSplitList ? k_attn_fwd<D, kSplitList> : k_attn_fwd<D, kSplitStream>;
+  HDP_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  kernel<<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
   note_launch();
   HDP_CUDA_TRY(cudaGetLastError());
   return HDP_OK;

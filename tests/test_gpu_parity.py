@@ -344,6 +344,24 @@ def test_seq128k_sampled(mode):
     sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq128k mode {mode}")
 
 
+def test_split_block_list_on_a_document_larger_than_l2():
+    """SPLIT streams FUSED's units (a partial at every chunk end) unless one
+    head's K and V rows of the longest document exceed 1.25x L2; then it runs
+    the block list (one unit per query tile of one (qc, kc) block).  Every
+    other SPLIT case here is short enough to stream.  A 393,216-token document
+    (48 chunks of 8,192; 201 MB of K and V per head at d = 128) and two short
+    ones, 2 query heads on 1 KV head, sampled rows against the oracle."""
+    lengths = [393216, 1000, 300]
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", None)
+    if l2:
+        assert 4 * (2 * max(lengths) * 128 * 2) > 5 * l2, "the input no longer reaches the block-list path"
+    w = wl.Workload("long-split", tuple(lengths), 8192, 2, 1, 128, 1.0, 5)
+    q, k, v = wl.qkv(w, device="cuda")
+    o, lse, plan = run_gpu(q, k, v, lengths, w.capacity, SPLIT)
+    toks, heads = sample_rows(lengths, w.hq, 60, 5)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, "block-list SPLIT")
+
+
 def test_mix1m_sampled():
     """1M-token skewed mixture, C = 8192, FUSED, sampled rows of every length class."""
     w = wl.workload("mix1m")
