@@ -89,9 +89,14 @@ def attn_kernel_source_sha256() -> str:
 # to the value it was captured with.
 PROFILED_TRAFFIC = {
     ("seq128k", "fused"): {
-        "kernel_source_sha256": "8c23a8430c8ada1741ac12010700bd2dacf6459bc08a3fe02fb6790ec27874d7",
-        "dram_bytes_per_launch": 5338317312 + 1069282304,
+        "kernel_source_sha256": "4e86f2afb84c3505bc11a8646696fcb7da983bd40007f35eb8ab557c4695ac66",
+        "dram_bytes_per_launch": 7911812352 + 1073514496,
         "source": "ncu capture summarised in profiles/attn_fwd_seq128k.md",
+    },
+    ("seq2m", "fused"): {
+        "kernel_source_sha256": "4e86f2afb84c3505bc11a8646696fcb7da983bd40007f35eb8ab557c4695ac66",
+        "dram_bytes_per_launch": 950496080640 + 17950700288,
+        "source": "single-pass ncu capture (DRAM bytes only) summarised in profiles/attn_fwd_seq2m_traffic.md",
     },
 }
 
@@ -411,7 +416,7 @@ def our_arm(args, ws, rank, local):
     flush = None if in_bytes > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    probe = pkg.hdp_plan_create(lengths_d, w.capacity)
+    probe = pkg.hdp_plan_create(lengths_d, w.capacity, flags=pkg.HDP_PLAN_NO_SPLIT)
     nshards = probe.view.num_shards
     ws_bytes = pkg.hdp_attention_workspace_bytes(probe, w.hq, w.d, mode)
     probe.destroy()
@@ -419,8 +424,8 @@ def our_arm(args, ws, rank, local):
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     attn_events = []
 
-    # a FUSED step needs no SPLIT work list
-    plan_flags = pkg.HDP_PLAN_NO_SPLIT if mode == pkg.HDP_MODE_FUSED else pkg.HDP_PLAN_DEFAULT
+    # neither attention mode walks the plan's SPLIT work list
+    plan_flags = pkg.HDP_PLAN_NO_SPLIT
 
     def step(record=False):
         plan = pkg.hdp_plan_create(lengths_d, w.capacity, flags=plan_flags, stream=stream)
@@ -618,9 +623,8 @@ def our_arm(args, ws, rank, local):
                          "peak_source": f"{src} bf16 dense burst",
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "attn_ms": attn_ms, "traffic": traffic,
-                         "traffic_note": None if traffic is not None else
-                         "no ncu capture of this kernel on this workload fits the capture size rule; "
-                         "see the seq128k entries"},
+                         "traffic_note": prof["source"] if traffic is not None else
+                         "no ncu capture of the current kernel source on this workload"},
             "cpu_baseline": cpu,
             "e2e": ({"value": job_throughput(job_flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,

@@ -64,9 +64,10 @@ typedef enum {
                                  shard_of_chunk = NULL); for callers that only
                                  need the attention tables */
 #define HDP_PLAN_NO_SPLIT 2u  /* skip the SPLIT work list (num_tiles_split = 0,
-                                 tiles_split = NULL); for callers that run FUSED
-                                 only.  SPLIT attention on such a plan fails
-                                 with INVALID_ARGUMENT */
+                                 tiles_split = NULL), a table for callers that
+                                 schedule blocks themselves; this library's
+                                 FUSED and SPLIT attention both walk the fused
+                                 list and run on such a plan unchanged */
 
 typedef struct hdp_plan_s* hdp_plan_t;
 
@@ -154,12 +155,14 @@ hdp_status_t hdp_attention_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t 
  *   FUSED: o and lse are final.  SPLIT: needs capacity % 128 == 0 and a
  *   workspace of hdp_attention_workspace_bytes; writes the partials there,
  *   then merges them into o and lse with hdp_lse_merge on the same stream.
- *   Each partial covers exactly its block's C keys.  The kernel either walks
- *   the SPLIT work list (a unit per block query tile) or walks the fused
- *   list and writes a partial at every chunk end of a query tile's key
- *   range; it takes the second unless one kv head's K and V rows of the
- *   longest document exceed 1.25x the device's L2.  Both give the same
- *   partials, bit for bit.
+ *   Each partial covers exactly its block's C keys: the kernel walks the
+ *   fused list and writes a partial at every chunk end of a query tile's
+ *   key range.
+ *   When one kv head's K and V rows of the longest document exceed the
+ *   device's L2, the CTAs of a launch pace each other along the key range so
+ *   that they share K/V tiles in L2.  Their positions go through one static
+ *   device table; concurrent launches share it, which can only weaken the
+ *   pacing (every hold is bounded) and never changes the results.
  *   q, k, v, o must be 16-byte aligned.
  * Device-side wait timeouts are reported by hdp_device_status.
  */

@@ -23,16 +23,24 @@
 // The online softmax keeps a stale running max unless it grows by more than
 // 2^8, so O is rescaled only rarely; the final O/l and LSE use the same max, so
 // the result is exact.  In SPLIT mode each block (q chunk, kv chunk) ends in a
-// partial (O fp32, LSE) instead, in one of two ways:
-//   block list  a unit is one query tile of one block (the plan's SPLIT work
-//               list): the unit's key range is that block's C keys
-//   streaming   a unit is FUSED's (a query tile over its whole causal key
-//               range); at each chunk boundary of that range the block just
-//               finished is written and the running max, l and O restart, so
-//               each partial still covers exactly its own C keys, without a
-//               unit restart (a new Q tile, a refilled pipeline) per block
-// The launch picks streaming unless one head's K and V rows of the longest
-// document are much larger than L2 (see launch()).
+// partial (O fp32, LSE) instead: the units are FUSED's (a query tile over its
+// whole causal key range), and at each chunk boundary of that range the block
+// just finished is written and the running max, l and O restart.  Each
+// partial covers exactly its own C keys, and no block restarts a unit (a new
+// Q tile, a refilled pipeline).
+//
+// Pacing (documents whose K and V rows of one head exceed L2): the CTAs of a
+// round stream the same K/V tiles, and they share them through L2 only while
+// they stay close together on the key range.  The SMs run at slightly
+// different speeds (about 2 % apart, steadily), so unpaced CTAs drift apart by
+// thousands of key tiles and each reads the tiles from HBM again.  So each
+// producer publishes its position on its K/V stream, a pacer warp reads the
+// positions of the other CTAs on the same stream, and the producer holds its
+// next load while it is more than a window ahead of the slowest.  The
+// kernel's duration was set by the slowest CTA anyway; what changes is that
+// the K/V tiles come from L2 (fewer HBM reads, so more of the power budget
+// for the SMs' clock).  Pacing is advisory: every hold is bounded, and it
+// never changes what is computed.
 //
 // Every mbarrier wait is bounded; a timeout sets the device error word, all
 // roles stop, in-flight copies and MMAs are drained, TMEM is freed.
@@ -40,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -51,6 +60,9 @@ namespace hdp {
 hdp_status_t launch_merge_blocks(const hdp_plan_s* plan, const float* o_part, const float* lse_part, int32_t hq,
                                  int32_t d, void* o, float* lse, cudaStream_t st);
 
+// Positions of the CTAs of a paced launch on their K/V streams (one slot per CTA).
+__device__ unsigned long long g_pace[1024];
+
 namespace {
 
 // 12 warps = 3 warpgroups: two softmax warpgroups and one for the producer
@@ -61,13 +73,14 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kPacerWarp = 10;
+constexpr int kPaceEvery = 8;    // key tiles between published positions
+constexpr int kPaceWindow = 24;  // key tiles a CTA may run ahead of the slowest on its stream
+constexpr unsigned int kPaceDone = 0xFFFFFFu;
 constexpr int kSoftmaxRegs = 176;
 constexpr int kControlRegs = 152;
 constexpr int kStages = 2;  // K and V ring depth
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
-// kernel modes (a template argument, so each mode's code carries no other
-// mode's state or branches: the FUSED softmax warps stay free of spills)
-constexpr int kFused = 0, kSplitList = 1, kSplitStream = 2;
 
 // error codes recorded in the device error word
 constexpr int kErrQFull = 0x101, kErrKFull = 0x102, kErrVFull = 0x103, kErrSFull = 0x104, kErrPFull = 0x105,
@@ -92,8 +105,11 @@ struct Bars {
   uint64_t k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;  // private to the MMA thread: completion of all its MMAs at exit
+  uint64_t pace_entry;  // this CTA's last published position (producer -> pacer)
+  uint64_t pace_limit;  // stream << 32 | furthest key tile the producer may load (pacer -> producer)
   uint32_t tmem_base;
   int abort_word;
+  int pace_done;        // the producer has finished
 };
 
 struct Params {
@@ -108,11 +124,13 @@ struct Params {
   float* o_part;         // SPLIT partials [N_b][C][hq][D]
   float* lse_part;       // SPLIT partials [N_b][hq][C]
   int C;
-  int tpc;               // streaming SPLIT: key tiles per chunk, C / 128
+  int tpc;               // SPLIT: key tiles per chunk, C / 128
   int ndocs;
-  const int32_t* cu;     // streaming SPLIT: cu_seqlens [ndocs + 1]
-  const int64_t* bo;     // streaming SPLIT: first causal block of each document [ndocs + 1]
+  const int32_t* cu;     // SPLIT: cu_seqlens [ndocs + 1]
+  const int64_t* bo;     // SPLIT: first causal block of each document [ndocs + 1]
   unsigned int* err;
+  unsigned long long* pace;  // per-CTA positions on the K/V streams, or nullptr: no pacing
+  unsigned int pace_epoch;   // 8 bits, distinct for consecutive launches
   long long wait_budget;  // clocks before a role's wait gives up (drain waits keep their own budget)
 };
 
@@ -191,11 +209,12 @@ __device__ __forceinline__ int doc_at(const int32_t* __restrict__ cu, int n, int
   return lo;
 }
 
-template <int D, int MODE>
+// SPLIT is a template argument, not a run-time flag, so the FUSED code carries
+// no SPLIT state or branches (its softmax warps stay free of register spills).
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
-  constexpr bool kSplit = MODE != kFused, kStream = MODE == kSplitStream;
   using L = SmemLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.drain, 1);
     bars.abort_word = 0;
+    bars.pace_entry = 0;
+    bars.pace_limit = 0;
+    bars.pace_done = 0;
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
@@ -314,9 +336,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hb = 0; hb < D / 64; ++hb)
             tma_load_3d(dst + hb * L::kHalfBytes, &tmQ, &bars.q_full[s], hb * 64, x.h0 + s, x.q_row0);
         }
+        // K/V stream of this unit: CTAs on the same stream read the same K/V tiles
+        const uint32_t stream = (static_cast<uint32_t>(x.kv_row0) * 2654435761u) ^ (static_cast<uint32_t>(x.kvh) + 1u);
+        const unsigned long long tag = (static_cast<unsigned long long>(stream) << 32) | ((p.pace_epoch & 0xFFu) << 24);
         if (ok) ok = arm_group(x, 0, -1);
-        for (int j = 0; j < x.ntiles_kv && ok; ++j) ok = arm_group(x, j + 1 < x.ntiles_kv ? j + 1 : -1, j);
+        for (int j = 0; j < x.ntiles_kv && ok; ++j) {
+          if (p.pace && (j % kPaceEvery) == 0) {
+            const unsigned long long e = tag | static_cast<unsigned int>(j);
+            *reinterpret_cast<volatile unsigned long long*>(p.pace + cta) = e;
+            *reinterpret_cast<volatile unsigned long long*>(&bars.pace_entry) = e;
+            // hold K(j+1) until the slowest CTA on this stream is within the window
+            const long long t0 = clock64();
+            for (;;) {
+              const unsigned long long lim = *reinterpret_cast<volatile unsigned long long*>(&bars.pace_limit);
+              if (static_cast<uint32_t>(lim >> 32) != stream || static_cast<unsigned int>(j) <= static_cast<unsigned int>(lim & 0xFFFFFFu))
+                break;
+              if (clock64() - t0 > p.wait_budget / 256 || *abort_word) break;  // advisory: give up and go on
+              __nanosleep(128);
+            }
+          }
+          ok = arm_group(x, j + 1 < x.ntiles_kv ? j + 1 : -1, j);
+        }
+        if (p.pace) {
+          const unsigned long long e = tag | kPaceDone;
+          *reinterpret_cast<volatile unsigned long long*>(p.pace + cta) = e;
+          *reinterpret_cast<volatile unsigned long long*>(&bars.pace_entry) = e;
+        }
       }
+      *reinterpret_cast<volatile int*>(&bars.pace_done) = 1;
       // Drain: every armed barrier's last phase completes once its bytes
       // land, so no copy into this CTA's shared memory is still in flight when
       // it exits, also when another role gave up after this loop ended.  In a
@@ -394,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key tile j of the unit; kind 0: steady (j < n - 2), 1: j = n - 2 (Q is
       // free after its S), 2: j = n - 1 (the unit's last P.V)
       // first / last: key tile j opens / closes an epilogue's span (the unit,
-      // or one C-key chunk in streaming SPLIT); call sites pass constants
+      // or one C-key chunk in SPLIT); call sites pass constants
       // where they can, so steady tiles carry no span bookkeeping
       auto tile = [&](const Unit& x, int nslots, int j, int vs, int ks, int kind, bool first, bool last) -> bool {
         for (int s = 0; s < nslots; ++s) {
@@ -438,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&bars.k_empty[c]);
         int j = 0;
-        if constexpr (kStream) {
+        if constexpr (SPLIT) {
           // span by span: the span's first tile, its steady middle (as in
           // FUSED: constant stages, no bookkeeping), then its last tile and
           // the unit's last two (kinds 1 and 2) with flags taken at run time
@@ -488,6 +535,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   } else {
+    if (warp == kPacerWarp && p.pace) {
+      // ---------------------------------------------------------- pacer
+      // Publishes, for this CTA's producer, the furthest key tile it may load:
+      // the least position among the CTAs of this launch on the same K/V
+      // stream, plus the window.  Ends with the producer, on an abort, or when
+      // this CTA's position has not moved for a whole wait budget.
+      // Lane 0 takes every decision and the warp follows it, so the whole warp
+      // reaches each shuffle and reduction together.
+      unsigned long long last = 0;
+      long long last_change = clock64();
+      for (;;) {
+        int stop = 0;
+        unsigned long long me = 0;
+        if (lane == 0) {
+          me = *reinterpret_cast<volatile unsigned long long*>(&bars.pace_entry);
+          stop = *reinterpret_cast<volatile int*>(&bars.pace_done) || *abort_word;
+          if (me != last) {
+            last = me;
+            last_change = clock64();
+          } else if (clock64() - last_change > p.wait_budget) {
+            stop = 1;
+          }
+        }
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        me = __shfl_sync(0xffffffffu, me, 0);
+        if (stop) break;
+        if (me != 0) {
+          const unsigned long long tag = me & ~0xFFFFFFull;
+          unsigned int mn = kPaceDone;
+          for (int i = lane; i < nctas; i += 32) {
+            const unsigned long long e = *reinterpret_cast<volatile unsigned long long*>(p.pace + i);
+            if ((e & ~0xFFFFFFull) == tag) mn = min(mn, static_cast<unsigned int>(e & 0xFFFFFFu));
+          }
+          mn = __reduce_min_sync(0xffffffffu, mn);
+          if (lane == 0) {
+            const unsigned int lim = mn >= kPaceDone - kPaceWindow ? kPaceDone : mn + kPaceWindow;
+            *reinterpret_cast<volatile unsigned long long*>(&bars.pace_limit) = (tag & ~0xFFFFFFFFull) | lim;
+          }
+        }
+        __syncwarp();
+        __nanosleep(256);
+      }
+    }
     named_barrier_sync(1, kThreads);  // the two idle warps of the control warpgroup
   }
   } else {
@@ -508,21 +598,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // doc-local query position relative to the first key of the range
       const int q_rel = x.q_row0 - x.kv_row0 + row;
       const int key_limit = min(q_rel + 1, x.kv_len);  // keys [0, key_limit) are allowed
-      // streaming SPLIT: the tile's chunk qc, its block (qc, 0), its first row
+      // SPLIT: the tile's chunk qc, its block (qc, 0), its first row
       // in the chunk
       int blk0 = 0, row0c = 0;
-      if constexpr (kStream) {
+      if constexpr (SPLIT) {
         const int doc = doc_at(p.cu, p.ndocs, x.kv_row0, lane);
         const int qc = x.row_off / p.C;
         blk0 = static_cast<int>(__ldg(p.bo + doc) + static_cast<long long>(qc) * (qc + 1) / 2);
         row0c = x.row_off - qc * p.C;
       }
       // key tiles in spans: the unit's whole range, or one C-key chunk in
-      // streaming SPLIT; each span ends in its own epilogue
-      const int nspan = kStream ? (x.ntiles_kv + p.tpc - 1) / p.tpc : 1;
+      // SPLIT; each span ends in its own epilogue
+      const int nspan = SPLIT ? (x.ntiles_kv + p.tpc - 1) / p.tpc : 1;
       for (int b = 0; b < nspan && ok; ++b) {
-        const int j0 = kStream ? b * p.tpc : 0;
-        const int j1 = kStream ? min(j0 + p.tpc, x.ntiles_kv) : x.ntiles_kv;
+        const int j0 = SPLIT ? b * p.tpc : 0;
+        const int j1 = SPLIT ? min(j0 + p.tpc, x.ntiles_kv) : x.ntiles_kv;
         float m = -INFINITY, l = 0.f;
         for (int j = j0; j < j1 && ok; ++j) {
           const bool first = j == j0;
@@ -656,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float inv_l = 1.f / l;
           const float lse_val = (m + __log2f(l)) * 0.69314718055994530942f;
           const long long tok = static_cast<long long>(x.q_row0) + row;
-          if constexpr (!kSplit) {
+          if constexpr (!SPLIT) {
             __nv_bfloat16* dst = p.o + (tok * p.hq + h) * static_cast<long long>(D);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -676,9 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (row_valid) p.lse[static_cast<long long>(h) * p.T + tok] = lse_val;
           } else {
-            const int blk = kStream ? blk0 + b : x.blk;
-            const int r0 = kStream ? row0c : x.row_off;  // the tile's first row in its chunk
-            const long long prow = static_cast<long long>(blk) * p.C + r0 + row;
+            const int blk = blk0 + b;
+            const long long prow = static_cast<long long>(blk) * p.C + row0c + row;
             float* dst = p.o_part + (prow * p.hq + h) * static_cast<long long>(D);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -693,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
               }
             }
-            if (row_valid) p.lse_part[(static_cast<long long>(blk) * p.hq + h) * p.C + r0 + row] = lse_val;
+            if (row_valid) p.lse_part[(static_cast<long long>(blk) * p.hq + h) * p.C + row0c + row] = lse_val;
           }
           tc_fence_before();
           __syncwarp();
@@ -763,23 +852,18 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   if ((r = make_map(&mq, q, T, hq, D)) != HDP_OK) return r;
   if ((r = make_map(&mk, k, T, hkv, D)) != HDP_OK) return r;
   if ((r = make_map(&mv, v, T, hkv, D)) != HDP_OK) return r;
-  // SPLIT: streaming unless one head's K and V rows of the longest document
-  // exceed 1.25x L2 (a bound between the two measured cases below).  Streaming units span whole key ranges, and the CTAs of a
-  // round share K/V tiles through L2 only while they stay close together on
-  // the range; the partial writes at chunk ends spread them out, and once the
-  // range no longer fits in L2 the shared tiles are read again from HBM.  The
-  // block list keeps every unit inside one chunk.  (Measured with C = 8,192,
-  // d = 128, one document: streaming was 4 % faster at 128K and 256K tokens,
-  // 134 MB of K and V, and 0.6 % slower at 384K tokens, 201 MB.)
+  // SPLIT walks the same fused units as FUSED.  Pacing when one head's K and
+  // V rows of the longest document exceed L2 (they no longer stay in L2 for
+  // a whole round on their own).
   int dev = 0, sms = 0, l2 = 0;
   HDP_CUDA_TRY(cudaGetDevice(&dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   HDP_CUDA_TRY(cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev));
   const long long kv_head_bytes = 2LL * plan->v.max_doc_len * D * 2;
-  const int mode = !split ? kFused : (4 * kv_head_bytes <= 5LL * l2 ? kSplitStream : kSplitList);
+  const bool pace = kv_head_bytes > l2;
   Params prm{};
-  prm.tiles = mode == kSplitList ? plan->v.tiles_split : plan->v.tiles_fused;
-  prm.ntiles = mode == kSplitList ? plan->v.num_tiles_split : plan->v.num_tiles_fused;
+  prm.tiles = plan->v.tiles_fused;
+  prm.ntiles = plan->v.num_tiles_fused;
   prm.hq = hq;
   prm.hkv = hkv;
   prm.group = hq / hkv;
@@ -798,14 +882,26 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   prm.err = device_error_word();
   if (!prm.err) return fail(HDP_ERR_CUDA, "cannot resolve the device error word");
   prm.wait_budget = wait_budget_clocks();
+  prm.pace = nullptr;
+  if (pace) {
+    static unsigned long long* pace_ptr[64] = {};
+    static std::atomic<unsigned int> epoch{0};
+    if (dev < 64 && !pace_ptr[dev]) {
+      void* a = nullptr;
+      HDP_CUDA_TRY(cudaGetSymbolAddress(&a, g_pace));
+      pace_ptr[dev] = static_cast<unsigned long long*>(a);
+    }
+    prm.pace = dev < 64 ? pace_ptr[dev] : nullptr;
+    prm.pace_epoch = epoch.fetch_add(1) % 255u + 1u;  // never 0: zeroed slots match no launch
+  }
   const long long units = prm.ntiles * hkv * prm.npairs;
   if (units == 0) return HDP_OK;
   const int grid = static_cast<int>(units < sms ? units : sms);
+  if (grid > 1024) prm.pace = nullptr;
   const long long bt = grid / (prm.npairs * heads_per_round(plan->v.max_doc_len, hkv));
   prm.block_tiles = bt > 0 ? bt : 1;
   const int smem = SmemLayout<D>::kBytes + 1024;
-  auto kernel = mode == kFused ? k_attn_fwd<D, kFused>
-               : mode == kSplitList ? k_attn_fwd<D, kSplitList> : k_attn_fwd<D, kSplitStream>;
+  auto kernel = split ? k_attn_fwd<D, true> : k_attn_fwd<D, false>;
   HDP_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   kernel<<<grid, kThreads, smem, st>>>(mq, mk, mv, prm);
   note_launch();
@@ -856,9 +952,7 @@ extern "C" hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const 
   float* o_part = nullptr;
   float* lse_part = nullptr;
   if (split) {
-    if (plan->flags & HDP_PLAN_NO_SPLIT)
-      return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT on a plan created with HDP_PLAN_NO_SPLIT");
-    if (plan->v.capacity % kTile != 0 || !plan->v.tiles_split)
+    if (plan->v.capacity % kTile != 0)
       return fail(HDP_ERR_INVALID_ARGUMENT, "hdp_attention_fwd: SPLIT needs capacity % 128 == 0");
     size_t ob = 0, need = 0;
     split_workspace(plan, hq, d, &ob, &need);

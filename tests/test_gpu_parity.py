@@ -78,7 +78,8 @@ def test_plan_create_blocks_the_host_once():
 
 def test_plan_without_split_list():
     """HDP_PLAN_NO_SPLIT leaves out the SPLIT work list only: every other table
-    is the default plan's, FUSED attention still runs, SPLIT is refused."""
+    is the default plan's, and FUSED and SPLIT attention (which walks the fused
+    list) give the default plan's results bit for bit."""
     lengths = [700, 130, 5, 1024, 77]
     dl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
     ref = oracle.plan(lengths, 256)
@@ -98,9 +99,10 @@ def test_plan_without_split_list():
             assert torch.equal(o, o2) and torch.equal(lse, lse2)
             ws = torch.empty(pkg.hdp_attention_workspace_bytes(full, w.hq, w.d, SPLIT), dtype=torch.uint8,
                              device="cuda")
-            with pytest.raises(pkg.HdpError) as e:
-                pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, SPLIT, ws, o2, lse2)
-            assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
+            pkg.hdp_attention_fwd(full, q, k, v, w.hq, w.hkv, w.d, w.scale, SPLIT, ws, o, lse)
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, SPLIT, ws, o2, lse2)
+            pkg.hdp_device_status()
+            assert torch.equal(o, o2) and torch.equal(lse, lse2)
     with pytest.raises(pkg.HdpError) as e:
         pkg.hdp_plan_create(dl, 256, flags=4)
     assert e.value.status == pkg.HDP_ERR_INVALID_ARGUMENT
@@ -344,22 +346,22 @@ def test_seq128k_sampled(mode):
     sampled_parity(w, q, k, v, o, lse, toks, heads, f"seq128k mode {mode}")
 
 
-def test_split_block_list_on_a_document_larger_than_l2():
-    """SPLIT streams FUSED's units (a partial at every chunk end) unless one
-    head's K and V rows of the longest document exceed 1.25x L2; then it runs
-    the block list (one unit per query tile of one (qc, kc) block).  Every
-    other SPLIT case here is short enough to stream.  A 393,216-token document
-    (48 chunks of 8,192; 201 MB of K and V per head at d = 128) and two short
-    ones, 2 query heads on 1 KV head, sampled rows against the oracle."""
+def test_split_paced_on_a_document_larger_than_l2():
+    """When one head's K and V rows of the longest document exceed L2, the
+    CTAs pace each other along the key range (FUSED's long-document tests
+    cover that too); here SPLIT, whose partial writes at every chunk end are
+    what spread unpaced CTAs apart.  A 393,216-token document (48 chunks of
+    8,192; 201 MB of K and V per head at d = 128) and two short ones, 2 query
+    heads on 1 KV head, sampled rows against the oracle."""
     lengths = [393216, 1000, 300]
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", None)
     if l2:
-        assert 4 * (2 * max(lengths) * 128 * 2) > 5 * l2, "the input no longer reaches the block-list path"
+        assert 2 * max(lengths) * 128 * 2 > l2, "the input no longer reaches the paced path"
     w = wl.Workload("long-split", tuple(lengths), 8192, 2, 1, 128, 1.0, 5)
     q, k, v = wl.qkv(w, device="cuda")
     o, lse, plan = run_gpu(q, k, v, lengths, w.capacity, SPLIT)
     toks, heads = sample_rows(lengths, w.hq, 60, 5)
-    sampled_parity(w, q, k, v, o, lse, toks, heads, "block-list SPLIT")
+    sampled_parity(w, q, k, v, o, lse, toks, heads, "paced SPLIT")
 
 
 def test_mix1m_sampled():
