@@ -161,8 +161,10 @@ hdp_status_t hdp_attention_workspace_bytes(hdp_plan_t plan, int32_t hq, int32_t 
  *   When one kv head's K and V rows of the longest document exceed the
  *   device's L2, the CTAs of a launch pace each other along the key range so
  *   that they share K/V tiles in L2.  Their positions go through one static
- *   device table; concurrent launches share it, which can only weaken the
- *   pacing (every hold is bounded) and never changes the results.
+ *   device table (its address cached per device, like the scratch of
+ *   hdp_attention_fwd_split_noalloc); concurrent launches share it, which can
+ *   only weaken the pacing (every hold is bounded) and never changes the
+ *   results.
  *   q, k, v, o must be 16-byte aligned.
  * Device-side wait timeouts are reported by hdp_device_status.
  */
@@ -186,8 +188,9 @@ hdp_status_t hdp_attention_fwd(hdp_plan_t plan, const void* q, const void* k, co
  *     call on a device resolves the scratch array's device address (once per
  *     device, with that device current) and caches it.  A cudaDeviceReset,
  *     or anything else that destroys the device's primary context,
- *     invalidates the cached address (and the device error word's): do not
- *     call the library on that device after such a reset in the same process.
+ *     invalidates the cached address (and those of the device error word and
+ *     the attention pacing table): do not call the library on that device
+ *     after such a reset in the same process.
  *   - Every call shares the one scratch array, which keeps the last call's
  *     contents; every partial a call reads is written by that call first, so
  *     nothing needs to start at zero.  Calls that overlap on the GPU (other
