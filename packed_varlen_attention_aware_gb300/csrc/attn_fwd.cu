@@ -843,6 +843,28 @@ hdp_status_t make_bf16_tile_map(CUtensorMap* m, const void* base, long long T, i
 
 namespace {
 
+// Pacing table of a device and the launch epochs, shared by every launch of
+// the library (both head sizes, all threads).  The table's address is
+// resolved once per device, on the first paced launch with that device
+// current; devices past the cache run unpaced.
+std::mutex g_pace_mu;
+unsigned long long* g_pace_ptr[64] = {nullptr};
+std::atomic<unsigned int> g_pace_epoch{0};
+
+hdp_status_t pace_table(int dev, unsigned long long** out) {
+  *out = nullptr;
+  if (dev < 0 || dev >= 64) return HDP_OK;
+  std::lock_guard<std::mutex> lk(g_pace_mu);
+  if (!g_pace_ptr[dev]) {
+    void* a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_pace);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(g_pace)");
+    g_pace_ptr[dev] = static_cast<unsigned long long*>(a);
+  }
+  *out = g_pace_ptr[dev];
+  return HDP_OK;
+}
+
 template <int D>
 hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const void* v, int hq, int hkv,
                     float scale, bool split, float* o_part, float* lse_part, void* o, float* lse, cudaStream_t st) {
@@ -884,15 +906,9 @@ hdp_status_t launch(const hdp_plan_s* plan, const void* q, const void* k, const 
   prm.wait_budget = wait_budget_clocks();
   prm.pace = nullptr;
   if (pace) {
-    static unsigned long long* pace_ptr[64] = {};
-    static std::atomic<unsigned int> epoch{0};
-    if (dev < 64 && !pace_ptr[dev]) {
-      void* a = nullptr;
-      HDP_CUDA_TRY(cudaGetSymbolAddress(&a, g_pace));
-      pace_ptr[dev] = static_cast<unsigned long long*>(a);
-    }
-    prm.pace = dev < 64 ? pace_ptr[dev] : nullptr;
-    prm.pace_epoch = epoch.fetch_add(1) % 255u + 1u;  // never 0: zeroed slots match no launch
+    hdp_status_t pr = pace_table(dev, &prm.pace);
+    if (pr != HDP_OK) return pr;
+    prm.pace_epoch = g_pace_epoch.fetch_add(1) % 255u + 1u;  // never 0: zeroed slots match no launch
   }
   const long long units = prm.ntiles * hkv * prm.npairs;
   if (units == 0) return HDP_OK;
