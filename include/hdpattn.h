@@ -97,7 +97,9 @@ typedef struct {
    * document length (fused list; 0 in the split list)}.  Fully masked
    * (cross-document or future) tiles never appear.  In the fused list the
    * rows of query tile j of a document also describe its key tile j (same
-   * rows), which the backward pass walks. */
+   * rows), which the backward pass walks.  Both attention modes walk the
+   * fused list; the split list is a table for callers that schedule one
+   * causal block at a time. */
   const int32_t* tiles_fused;    /* [num_tiles_fused][8] one per document query tile */
   int64_t num_tiles_fused;
   const int32_t* tiles_split;    /* [num_tiles_split][8] one per block query tile
