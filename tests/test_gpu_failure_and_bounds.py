@@ -108,6 +108,87 @@ def test_backward_expired_wait_reports_timeout_and_the_next_call_recovers():
         assert err.max() <= 2e-2 * np.abs(ref).max() + 1e-6, name
 
 
+# ---------------------------------------------------------------- pacing
+# A 327,680-token document: one kv head's K and V rows (168 MB at d = 128)
+# exceed L2, so the forward's CTAs pace each other through the library's
+# static position table.  Two query heads on one kv head keep it cheap.
+LONG = 327680
+
+
+def _long_case(seed):
+    w = wl.Workload("paced", (LONG,), 8192, 2, 1, 128, 1.0, seed)
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", None)
+    if l2:
+        assert 2 * LONG * w.d * 2 > l2, "the input no longer reaches the paced path"
+    q, k, v = wl.qkv(w, device="cuda")
+    return w, q, k, v
+
+
+def test_paced_launch_expired_wait_reports_timeout_and_the_next_call_recovers():
+    """A paced launch whose waits expire at once: the pacer warp stops with
+    its CTA, the kernel returns, the status reads HDP_ERR_DEVICE_TIMEOUT, and
+    the next call on the same plan passes parity."""
+    w, q, k, v = _long_case(21)
+    dl = torch.tensor(w.lengths, dtype=torch.int32, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros((w.hq, LONG), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    pkg.hdp_device_status()
+    with pkg.hdp_plan_create(dl, w.capacity, flags=pkg.HDP_PLAN_NO_SPLIT) as plan:
+        pkg.hdp_set_wait_budget(1)
+        try:
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, FUSED, None, o, lse)
+            torch.cuda.synchronize()
+        finally:
+            pkg.hdp_set_wait_budget(0)
+        with pytest.raises(pkg.HdpError) as e:
+            pkg.hdp_device_status()
+        assert e.value.status == pkg.HDP_ERR_DEVICE_TIMEOUT
+        pkg.hdp_device_status()
+        pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, FUSED, None, o, lse)
+        pkg.hdp_device_status()
+    toks, heads = sample_rows(list(w.lengths), w.hq, 40, 21)
+    sampled_parity(w, q, k, v, o, lse, toks, heads, "paced, after a timeout")
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_concurrent_paced_launches_match_lone_launches(mode):
+    """Launches in flight together on two streams share the pacing table; each
+    must give its lone launch's output bit for bit."""
+    cases = [_long_case(31), _long_case(32)]
+    outs, plans, wss = [], [], []
+    for w, q, k, v in cases:
+        dl = torch.tensor(w.lengths, dtype=torch.int32, device="cuda")
+        plan = pkg.hdp_plan_create(dl, w.capacity, flags=pkg.HDP_PLAN_NO_SPLIT)
+        wsb = pkg.hdp_attention_workspace_bytes(plan, w.hq, w.d, mode)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+        plans.append(plan)
+        wss.append(ws)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.hq, LONG), dtype=torch.float32, device="cuda")
+        pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, mode, ws, o, lse)
+        outs.append((o, lse))
+    pkg.hdp_device_status()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = []
+    torch.cuda.synchronize()
+    for (w, q, k, v), plan, st in zip(cases, plans, streams):
+        o = torch.empty_like(q)
+        lse = torch.empty((w.hq, LONG), dtype=torch.float32, device="cuda")
+        got.append((o, lse))
+    for rep in range(2):  # two launches per stream, all enqueued before any wait
+        for i, ((w, q, k, v), plan, st) in enumerate(zip(cases, plans, streams)):
+            # the two streams need separate SPLIT workspaces: each case has its own
+            pkg.hdp_attention_fwd(plan, q, k, v, w.hq, w.hkv, w.d, w.scale, mode, wss[i], got[i][0], got[i][1],
+                                  stream=st)
+    torch.cuda.synchronize()
+    pkg.hdp_device_status()
+    for (o, lse), (o2, lse2) in zip(outs, got):
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    for plan in plans:
+        plan.destroy()
+
+
 # ---------------------------------------------------------------- guard bands
 
 def _guarded(nbytes):
