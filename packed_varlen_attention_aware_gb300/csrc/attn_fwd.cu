@@ -336,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hb = 0; hb < D / 64; ++hb)
             tma_load_3d(dst + hb * L::kHalfBytes, &tmQ, &bars.q_full[s], hb * 64, x.h0 + s, x.q_row0);
         }
-        // K/V stream of this unit: CTAs on the same stream read the same K/V tiles
+        // K/V stream of this unit: CTAs on the same stream read the same K/V
+        // tiles.  A published position is stream hash (bits 63-32) | launch
+        // epoch (31-24) | key tile (23-0, kPaceDone once the unit is done).
         const uint32_t stream = (static_cast<uint32_t>(x.kv_row0) * 2654435761u) ^ (static_cast<uint32_t>(x.kvh) + 1u);
         const unsigned long long tag = (static_cast<unsigned long long>(stream) << 32) | ((p.pace_epoch & 0xFFu) << 24);
         if (ok) ok = arm_group(x, 0, -1);
