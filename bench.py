@@ -512,7 +512,7 @@ def our_arm(args, ws, rank, local):
         def upload(i):
             b = i & 1
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_out[b])  # the slot's previous outputs are home, its inputs no longer read
+                s_in.wait_event(ev_done[b])  # the slot's inputs are no longer read: its last compute is done
                 qd[b].copy_(qh, non_blocking=True)
                 kd[b].copy_(kh, non_blocking=True)
                 vd[b].copy_(vh, non_blocking=True)
@@ -522,6 +522,7 @@ def our_arm(args, ws, rank, local):
         def compute_and_download(i):
             b = i & 1
             stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])  # the slot's previous outputs are home before they are overwritten
             plan = pkg.hdp_plan_create(ld[b], w.capacity, flags=plan_flags, stream=stream)
             pkg.hdp_attention_fwd(plan, qd[b], kd[b], vd[b], w.hq, w.hkv, w.d, w.scale, mode, workspace, od[b], lsed[b],
                                   stream=stream)
@@ -544,6 +545,7 @@ def our_arm(args, ws, rank, local):
 
         for b in range(2):
             ev_out[b].record(s_out)
+            ev_done[b].record(stream)
         e2e_run(e2e_warm)
         torch.cuda.synchronize()
         if ws > 1:
